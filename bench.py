@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Throughput of the Beam MoE sublayer on GB300.
+
+One step = one pass of the whole sublayer (boundary norm -> FP32 router and
+group top-k -> permutation -> gate/up GEMM with SwiGLU -> down GEMM ->
+combine) over one batch of synthetic tokens, through the C ABI
+(beam_moe_layer). Default workload: the decode batch of one token at Beam
+shapes (hidden 5120, 256 experts in 8 groups, top 4 groups / top 8 experts,
+d_ff 2560, n = 20).
+
+Timing: W untimed warm-up steps, then K steps. Before each step a 512 MB
+buffer is overwritten (L2 is 129 MB) and the input batch rotates over
+``--batches`` seeded draws, so expert weights come from HBM; CUDA events
+recorded by the library at the stage boundaries time each step and each
+kernel on the launching stream. The flush is outside the events.
+
+Prints one JSON line (rank 0). Multi-GPU (torchrun): every rank runs the same
+workload on its own GPU (tokens are independent: replicas, weak scaling); the
+value is all ranks' tokens over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle on the same workload instead
+(one token per step, host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from beam_inputs import CONFIGS, make_activations, make_norm_weights, make_router  # noqa: E402
+
+METRIC = "MoE-sublayer tokens/s on 1 GB300 + % of HBM (decode) / bf16 TC (prefill) roofline"
+UNIT = "tokens/s"
+STAGES = ["boundary", "router_topk", "permute", "gate_up", "down", "combine"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="decode_t1", choices=sorted(CONFIGS))
+    p.add_argument("--batches", type=int, default=16, help="seeded input batches to rotate over")
+    p.add_argument("--num-experts", type=int, default=None,
+                   help="override E (same per-expert shapes; for small-footprint profiling runs)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    args = p.parse_args(argv)
+    if args.num_experts is not None:
+        CONFIGS[args.config] = CONFIGS[args.config].with_(E=args.num_experts)
+    if args.steps is None:
+        args.steps = 500 if CONFIGS[args.config].T <= 64 else 20
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    return args
+
+
+# ---------------------------------------------------------------- multi-process helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def whole_job(tokens_per_rank: int, world: int, rank_seconds: list) -> tuple:
+    """Weak scaling: every rank processes its own tokens; the job takes as
+    long as its slowest rank. Returns (tokens/s, slowest seconds)."""
+    slowest = max(rank_seconds)
+    return tokens_per_rank * world / slowest, slowest
+
+
+def reduce_max(value: float, device) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock, power and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.gpu_id, self.period = gpu_id, period_ms
+        self.lines, self.proc, self.thread = [], None, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", self.gpu_id, "-lms", str(self.period)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[device_index]
+        return str(device_index)
+
+
+# ---------------------------------------------------------------- peaks and traffic
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if one matches this kernel build."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    for line in text.splitlines():
+        if line.strip().startswith("dram_bytes_per_launch:"):
+            try:
+                return float(line.split(":", 1)[1].split()[0])
+            except ValueError:
+                return None
+    return None
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(cfg, seconds: float, max_tokens: int, fixed_batch: bool = False):
+    """Times the fp64 oracle on tokens of this workload until ~`seconds` have
+    passed. Returns (tokens, elapsed seconds, worker threads)."""
+    from beam_inputs import expert_weights
+    from oracle import bf16 as obf
+    from oracle.layer import layer
+    workers = max(1, len(os.sched_getaffinity(0)))
+    wp, wq = make_norm_weights(cfg)
+    W_r, bias = make_router(cfg)
+    cache = {}
+
+    def expert_fn(e):
+        if e not in cache:
+            cache[e] = tuple(obf.decode(m) for m in expert_weights(cfg, e))
+        return cache[e]
+
+    done, elapsed, b = 0, 0.0, 0
+    while done < max_tokens and elapsed < seconds:
+        h, x = make_activations(cfg.with_(T=1), batch=0 if fixed_batch else b)
+        if not fixed_batch:
+            cache.clear()
+        t0 = time.perf_counter()
+        layer(obf.decode(h), obf.decode(x), obf.decode(wp), obf.decode(wq), W_r, bias, n=cfg.n, eps=cfg.eps,
+              G=cfg.G, TG=cfg.TG, K=cfg.K, routed_scale=cfg.routed_scale, expert_fn=expert_fn, workers=workers)
+        elapsed += time.perf_counter() - t0
+        done += 1
+        b += 1
+    return done, elapsed, workers
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = CONFIGS[args.config]
+    from beam_inputs import expert_weights
+    from oracle import bf16 as obf
+    from oracle.layer import layer
+    workers = max(1, len(os.sched_getaffinity(0)))
+    wp, wq = make_norm_weights(cfg)
+    W_r, bias = make_router(cfg)
+    cache = {}
+
+    def expert_fn(e):
+        if e not in cache:
+            cache[e] = tuple(obf.decode(m) for m in expert_weights(cfg, e))
+        return cache[e]
+
+    h, x = make_activations(cfg.with_(T=1), batch=0)
+    args_l = (obf.decode(h), obf.decode(x), obf.decode(wp), obf.decode(wq), W_r, bias)
+    kw = dict(n=cfg.n, eps=cfg.eps, G=cfg.G, TG=cfg.TG, K=cfg.K, routed_scale=cfg.routed_scale,
+              expert_fn=expert_fn, workers=workers)
+    for _ in range(args.warmup):
+        layer(*args_l, **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        layer(*args_l, **kw)
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    sample = (f"1 token of {cfg.name} per step (the workload's seed-0 token, its 8 experts decoded to fp64 "
+              f"once and reused), fp64 numpy oracle, {workers} worker threads")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "G": cfg.G, "TG": cfg.TG,
+                      "K": cfg.K, "F": cfg.F, "n": cfg.n},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our implementation
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    import routed_expert_layer_post_gb300 as beam
+    from routed_expert_layer_post_gb300 import build as beam_build
+    beam_build.build()
+    lib = beam.library()
+
+    cfg = CONFIGS[args.config]
+    T, H, E, F = cfg.T, cfg.H, cfg.E, cfg.F
+    mc = beam.make_config(H, E, cfg.G, cfg.TG, cfg.K, F, cfg.routed_scale, cfg.eps)
+
+    # expert weights: bf16 N(0, 1/sqrt(fan_in)) drawn on the device with a seeded generator
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1000 + cfg.seed)
+    w_gu = torch.empty(E, 2 * F, H, dtype=torch.bfloat16, device=device)
+    w_d = torch.empty(E, H, F, dtype=torch.bfloat16, device=device)
+    for e in range(E):
+        w_gu[e].copy_(torch.randn(2 * F, H, device=device, generator=gen) / H ** 0.5)
+        w_d[e].copy_(torch.randn(H, F, device=device, generator=gen) / F ** 0.5)
+
+    def bf(a):
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+
+    wp, wq = make_norm_weights(cfg)
+    W_r, bias = make_router(cfg)
+    tens = dict(w_post=bf(wp), w_pre=bf(wq), router_w=torch.from_numpy(W_r).to(device),
+                bias=torch.from_numpy(bias).to(device), w_gate_up=w_gu, w_down=w_d)
+    weights = beam.weights_struct(**tens)
+
+    B = max(1, args.batches)
+    hs, xs, hs_host, xs_host = [], [], [], []
+    for b in range(B):
+        hb, xb = make_activations(cfg, batch=b)
+        hs.append(bf(hb))
+        xs.append(bf(xb))
+        if not args.no_e2e:
+            hs_host.append(torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory())
+            xs_host.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory())
+    h_out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    y_out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=device)
+    ws_bytes = lib.beam_moe_workspace_size(ctypes.byref(mc), T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sp = stream.cuda_stream
+
+    K, W = args.steps, args.warmup
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for evs in events:
+        for ev in evs:
+            ev.record(stream)          # materialise the handles
+    dbgs = []
+    for evs in events:
+        d = beam.MoeDebug()
+        d.expert_offsets = offs.data_ptr()
+        for i, ev in enumerate(evs):
+            d.stage_events[i] = ev.cuda_event
+        dbgs.append(d)
+    dbg_plain = beam.MoeDebug()
+    dbg_plain.expert_offsets = offs.data_ptr()
+    torch.cuda.synchronize()
+
+    def step(i, dbg):
+        b = i % B
+        st = lib.beam_moe_layer(hs[b].data_ptr(), xs[b].data_ptr(), cfg.n, ctypes.byref(weights), T,
+                                ctypes.byref(mc), h_out.data_ptr(), y_out.data_ptr(), ctypes.byref(dbg),
+                                ws.data_ptr(), ws_bytes, sp)
+        if st != 0:
+            raise RuntimeError(f"beam_moe_layer: {beam.beam_status_string(st)}")
+
+    # warm-up; also records how many experts each batch touches
+    touched = []
+    for i in range(max(W, B)):
+        flush.zero_()
+        step(i, dbg_plain)
+        if i < B:
+            touched.append(int((torch.diff(offs) > 0).sum().item()))
+    launches_per_step = lib.beam_last_launch_count()
+    torch.cuda.synchronize()
+    if lib.beam_get_device_error(ctypes.byref(ctypes.c_int(0)), ctypes.c_void_p(sp)) != 0:
+        raise RuntimeError("device wait timed out during warm-up")
+
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id_for(device.index)) as clocks:
+        for i in range(K):
+            flush.zero_()
+            step(i, dbgs[i])
+        torch.cuda.synchronize()
+    barrier()
+
+    step_ms = [events[i][0].elapsed_time(events[i][6]) for i in range(K)]
+    stage_ms = {s: [events[i][j].elapsed_time(events[i][j + 1]) for i in range(K)] for j, s in enumerate(STAGES)}
+    total_s = sum(step_ms) / 1e3
+    slowest = reduce_max(total_s, device)
+    value, slowest = whole_job(T * K, world, [slowest])
+
+    # roofline of the dominant kernel (by mean time)
+    peaks, peaks_kind = load_peaks()
+    mean_stage = {s: statistics.fmean(v) for s, v in stage_ms.items()}
+    dom = max(("gate_up", "down"), key=lambda s: mean_stage[s])
+    rows = T * cfg.K
+    touched_per_step = [touched[i % B] for i in range(K)]
+    if dom == "gate_up":
+        w_bytes = 2 * F * H * 2
+        act_bytes = rows * H * 2 + rows * F * 2
+        flops = 2.0 * rows * 2 * F * H
+    else:
+        w_bytes = H * F * 2
+        act_bytes = rows * F * 2 + rows * H * 2
+        flops = 2.0 * rows * H * F
+    bytes_total = sum(tc * w_bytes + act_bytes for tc in touched_per_step)
+    dom_s = sum(stage_ms[dom]) / 1e3
+    t_hbm = bytes_total / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops * K / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = bytes_total / dom_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = flops * K / dom_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    roof.update({"traffic": profiled_traffic(dom, cfg.name), "kernel": dom, "peak_source": peaks_kind,
+                 "algorithmic_bytes_per_launch": bytes_total / K, "launch_us": 1e3 * statistics.fmean(stage_ms[dom])})
+
+    # end to end through the host-buffer entry point: H2D of h, x and D2H of h', y inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hbytes = lib.beam_moe_layer_host_workspace_size(ctypes.byref(mc), T)
+        ws_h = torch.empty(hbytes, dtype=torch.uint8, device=device)
+        ho = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        yo = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        Ke = min(K, 200)
+        tot = 0.0
+        for i in range(Ke + 3):
+            flush.zero_()
+            torch.cuda.synchronize()
+            b = i % B
+            t0 = time.perf_counter()
+            st = lib.beam_moe_layer_host(hs_host[b].data_ptr(), xs_host[b].data_ptr(), cfg.n,
+                                         ctypes.byref(weights), T, ctypes.byref(mc), ho.data_ptr(), yo.data_ptr(),
+                                         ws_h.data_ptr(), hbytes, sp)
+            dt = time.perf_counter() - t0
+            if st != 0:
+                raise RuntimeError(f"beam_moe_layer_host: {beam.beam_status_string(st)}")
+            if i >= 3:
+                tot += dt
+        tot = reduce_max(tot, device)
+        e2e = {"value": T * Ke * world / tot, "unit": UNIT, "h2d_bytes_per_step": 2 * T * H * 2,
+               "d2h_bytes_per_step": 2 * T * H * 2, "steps": Ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, el, workers = oracle_sample(cfg, args.cpu_seconds, max_tokens=64)
+        cpu = {"value": tok / el, "unit": UNIT, "cores": workers, "kind": "oracle",
+               "sample": f"{tok} tokens of {cfg.name} (one per seeded batch, experts decoded to fp64 per token), "
+                         f"fp64 numpy oracle, {workers} worker threads, {el:.1f} s"}
+
+    if rank == 0:
+        clk = clocks.summary()
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+               "ms_per_step": 1e3 * slowest / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "G": cfg.G, "TG": cfg.TG, "K": cfg.K,
+                          "F": F, "n": cfg.n, "parallelism": f"replicas x{world}",
+                          "l2": "512 MB buffer overwritten before every step (outside the timed events); "
+                                f"inputs rotate over {B} seeded batches",
+                          "weights": "expert weights bf16 N(0, 1/sqrt(fan_in)) drawn on the device; router, "
+                                     "norms, bias and activations from beam_inputs"},
+               "us_per_layer": 1e3 * statistics.fmean(step_ms),
+               "stage_us": {s: round(1e3 * statistics.fmean(v), 2) for s, v in stage_ms.items()},
+               "touched_experts_mean": statistics.fmean(touched_per_step),
+               "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": launches_per_step * K, "clocks": clk}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,206 @@
+/*
+ * beam.h -- C ABI of libbeam.so: the Beam 501B-A23B MoE sublayer at a
+ * sandwich-norm boundary, as hand-written CUDA kernels for one GB300 (sm_103a).
+ *
+ * The method comes from three public pages about serving Reflection Beam:
+ * the TokenSpeed blog on Reflection Beam (lightseek.org), the Gaudi cookbook
+ * port "Beam-1.0-501B-A23B on Gaudi 2", and a summary of the vLLM Beam post
+ * (agentlenshq). Each entry point below names the section that defines its
+ * operation.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - bf16 tensors are passed as uint16_t bit patterns (bfloat16), fp32 tensors
+ *   as float, indices as int32_t. All tensors are dense and row-major; the
+ *   last index is contiguous.
+ * - Every tensor pointer is a DEVICE pointer owned by the caller, except in
+ *   beam_moe_layer_host, which also takes host buffers. The library never
+ *   allocates device memory and keeps no per-call state; scratch memory comes
+ *   from the caller's workspace (`ws`, `ws_bytes`, sized by the *_workspace_size
+ *   queries, 256-byte aligned, no initial contents required).
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). All work is enqueued on it; no entry point synchronises, except
+ *   beam_moe_layer_host and beam_get_device_error.
+ * - Argument errors are detected on the host before anything is launched and
+ *   return a status other than BEAM_OK; nothing is enqueued in that case.
+ *   A launch failure returns BEAM_ERR_CUDA. Asynchronous device errors show up
+ *   in later CUDA calls; a timed-out bounded wait inside a kernel is reported
+ *   by beam_get_device_error.
+ * - T == 0 is a valid empty batch: the call checks its config and returns
+ *   BEAM_OK without launching anything.
+ * - Alignment: every bf16 and fp32 tensor must be 16-byte aligned (128-bit
+ *   vector loads and TMA); int32 tensors 4-byte aligned.
+ * - Supported shapes: H % 256 == 0 and H <= 8192; F % 128 == 0; E <= 256;
+ *   E % G == 0; G <= 32; E/G <= 32; 1 <= TG <= G; 1 <= K <= 16;
+ *   K <= TG * E/G; T * K < 2^31.
+ */
+#ifndef BEAM_H
+#define BEAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BEAM_OK = 0,
+  BEAM_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad config value */
+  BEAM_ERR_MISALIGNED = 2,          /* pointer not aligned as the conventions require */
+  BEAM_ERR_UNSUPPORTED_SHAPE = 3,   /* shape outside the supported set above */
+  BEAM_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the matching *_workspace_size */
+  BEAM_ERR_CUDA = 5,                /* a CUDA runtime call or kernel launch failed */
+  BEAM_ERR_DEVICE_TIMEOUT = 6,      /* a bounded wait inside a kernel gave up */
+  BEAM_ERR_UNSUPPORTED_DEVICE = 7   /* current device is not compute capability 10.3 */
+} beam_status_t;
+
+/* Shape and scalars of one MoE sublayer. Beam: hidden 5120, 256 experts in 8
+ * groups, top 4 groups, top 8 experts, d_ff 2560, routed scale 2.5, eps 1e-6
+ * (vLLM Beam summary, "MoE and residual stream"; TokenSpeed blog,
+ * "Model architecture and precision -> Architecture"). */
+typedef struct {
+  int hidden;          /* H */
+  int num_experts;     /* E */
+  int num_groups;      /* G: contiguous groups of E/G experts */
+  int topk_groups;     /* TG */
+  int topk;            /* K */
+  int d_ff;            /* F */
+  float routed_scale;  /* 2.5 for Beam */
+  float eps;           /* RMSNorm epsilon */
+} beam_moe_config_t;
+
+/* Weights of one MoE sublayer (all device pointers). */
+typedef struct {
+  const uint16_t* w_post;     /* bf16 [H]: RMSNorm weight after the previous sublayer */
+  const uint16_t* w_pre;      /* bf16 [H]: RMSNorm weight before this MoE sublayer */
+  const float* router_w;      /* fp32 [E][H] (one row per expert) */
+  const float* bias;          /* fp32 [E]: correction bias, used for selection only */
+  const uint16_t* w_gate_up;  /* bf16 [E][2F][H]: rows 0..F-1 gate, rows F..2F-1 up */
+  const uint16_t* w_down;     /* bf16 [E][H][F] */
+} beam_moe_weights_t;
+
+/* Optional intermediate outputs of beam_moe_layer (each may be NULL). */
+typedef struct {
+  uint16_t* z;              /* bf16 [T][H]: pre-normed MoE input */
+  float* logits;            /* fp32 [T][E]: router logits */
+  int32_t* topk_ids;        /* int32 [T][K] */
+  float* topk_w;            /* fp32 [T][K] */
+  int32_t* expert_offsets;  /* int32 [E+1] */
+  /* Optional cudaEvent_t handles (as void*, NULL to skip) recorded on the
+   * stream at the stage boundaries: [0] before the boundary norm, [1] after
+   * it, [2] after router + top-k, [3] after the permutation, [4] after the
+   * gate/up GEMM, [5] after the down GEMM, [6] after the combine. Used for
+   * per-kernel timing; the events are created and owned by the caller. */
+  void* stage_events[7];
+} beam_moe_debug_t;
+
+const char* beam_status_string(beam_status_t status);
+const char* beam_version(void);
+
+/* Sandwich-norm boundary (vLLM Beam summary, "MoE and residual stream" and
+ * kernel change 1; TokenSpeed blog, "MNNVL all-reduce and SandwichNorm
+ * fusion"; Gaudi cookbook port, "What was built -> Model code"):
+ *   y  = bf16(x / sqrt(mean(x^2) + eps) * w_post)
+ *   h' = bf16(sqrt((n-1)/n) * h + y / sqrt(n))
+ *   z  = bf16(h' / sqrt(mean(h'^2) + eps) * w_pre)
+ * in FP32 math with the three bf16 rounding points shown. h, x: [T][H];
+ * h_out, z_out: [T][H]. h_out may alias h (in-place update of the residual);
+ * no other aliasing. n >= 1 is the 1-based index of this residual add. */
+beam_status_t beam_boundary_norm(const uint16_t* h, const uint16_t* x, const uint16_t* w_post,
+                                 const uint16_t* w_pre, int T, int H, float eps, int n,
+                                 uint16_t* h_out, uint16_t* z_out, void* stream);
+
+/* FP32 router and group-limited top-k (TokenSpeed blog, "Fused FP32
+ * routing" and "Model architecture and precision -> Architecture"; vLLM Beam
+ * summary, "MoE and residual stream"; Gaudi cookbook port, "Model code"):
+ *   logits = z W_r^T with fp32 FMA (no TF32, no bf16), s = sigmoid(logits),
+ *   s' = s + bias; group score = sum of the two largest s' in each group of
+ *   E/G contiguous experts; the TG best groups, then the K best s' inside
+ *   them (ties to the lower index); slots in descending s';
+ *   topk_w[t][k] = routed_scale * s_k / sum_j s_j (unbiased scores).
+ * z: bf16 [T][H]; router_w fp32 [E][H]; bias fp32 [E]; logits_out fp32 [T][E]
+ * (required: it also serves as the scores buffer); topk_ids int32 [T][K];
+ * topk_w fp32 [T][K]. */
+beam_status_t beam_router_topk(const uint16_t* z, const float* router_w, const float* bias, int T,
+                               const beam_moe_config_t* cfg, float* logits_out, int32_t* topk_ids,
+                               float* topk_w, void* stream);
+
+/* Permutation by expert (vLLM Beam summary, "The fused decoding graph runs
+ * one MoE layer in 13 kernels": routing kernels feed grouped GEMMs). The T*K
+ * pairs i = t*K + k are ordered by (expert, t): a stable counting sort built
+ * from a histogram and an exclusive prefix scan, with no atomics deciding the
+ * order. Outputs: expert_offsets int32 [E+1] (offsets[e]..offsets[e+1] are
+ * expert e's rows), perm_token int32 [T*K] (token of each permuted row),
+ * inv_perm int32 [T*K] (row of pair i), and, if x_perm is not NULL,
+ * x_perm bf16 [T*K][H] with x_perm[p] = z[perm_token[p]]. */
+size_t beam_moe_permute_workspace_size(const beam_moe_config_t* cfg, int T);
+beam_status_t beam_moe_permute(const int32_t* topk_ids, const uint16_t* z, int T,
+                               const beam_moe_config_t* cfg, int32_t* expert_offsets,
+                               int32_t* perm_token, int32_t* inv_perm, uint16_t* x_perm, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* Routed SwiGLU experts and weighted combine (TokenSpeed blog, "TensorRT-LLM
+ * NVFP4 MoE": both expert GEMMs, SwiGLU fused into the first, weighted sum of
+ * expert outputs per token; vLLM Beam summary: 256 experts, d_ff 2560):
+ *   act[p]  = bf16(silu(x_perm[p] W_g^T) * (x_perm[p] W_u^T))   (gate/up GEMM)
+ *   y_perm[p] = bf16(act[p] W_d^T)                              (down GEMM)
+ *   y[t]   = bf16(sum_k topk_w[t][k] * y_perm[inv_perm[t*K+k]]) (combine, k in order)
+ * for the expert e that owns row p. Grouped GEMMs on tcgen05 tensor cores with
+ * fp32 accumulation in tensor memory, fed by TMA. The combine is atomic-free
+ * and deterministic. y_out: bf16 [T][H]. */
+size_t beam_moe_experts_workspace_size(const beam_moe_config_t* cfg, int T);
+beam_status_t beam_moe_experts(const uint16_t* x_perm, const int32_t* expert_offsets,
+                               const uint16_t* w_gate_up, const uint16_t* w_down,
+                               const float* topk_w, const int32_t* inv_perm, int T,
+                               const beam_moe_config_t* cfg, uint16_t* y_out, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* The three stages of beam_moe_experts, exposed for inspection and for timing
+ * each kernel on its own. act: bf16 [T*K][F]; y_perm: bf16 [T*K][H].
+ * beam_moe_gate_up and beam_moe_down need beam_moe_experts_workspace_size
+ * bytes of workspace (their split-K partial sums). */
+beam_status_t beam_moe_gate_up(const uint16_t* x_perm, const int32_t* expert_offsets,
+                               const uint16_t* w_gate_up, int T, const beam_moe_config_t* cfg,
+                               uint16_t* act, void* ws, size_t ws_bytes, void* stream);
+beam_status_t beam_moe_down(const uint16_t* act, const int32_t* expert_offsets,
+                            const uint16_t* w_down, int T, const beam_moe_config_t* cfg,
+                            uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream);
+beam_status_t beam_moe_combine(const uint16_t* y_perm, const float* topk_w, const int32_t* inv_perm,
+                               int T, const beam_moe_config_t* cfg, uint16_t* y_out, void* stream);
+
+/* The whole sublayer: boundary -> router/top-k -> permutation -> experts ->
+ * combine, as stream-ordered launches. Inputs: residual h and previous
+ * sublayer output x, bf16 [T][H]; n = index of this residual add. Outputs:
+ * the new residual h_out and the MoE output y_out (the next boundary's x),
+ * bf16 [T][H]. h_out may alias h. dbg may be NULL. */
+size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int T);
+beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n,
+                             const beam_moe_weights_t* weights, int T,
+                             const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
+                             const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream);
+
+/* beam_moe_layer with HOST input and output buffers: copies h and x (host,
+ * pinned memory recommended) into the workspace, runs the layer, copies h_out
+ * and y_out back to the host buffers, and synchronises the stream before it
+ * returns. Weights stay device pointers. Workspace: beam_moe_layer_host_workspace_size. */
+size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T);
+beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
+                                  const beam_moe_weights_t* weights, int T,
+                                  const beam_moe_config_t* cfg, uint16_t* h_out_host,
+                                  uint16_t* y_out_host, void* ws, size_t ws_bytes, void* stream);
+
+/* Reads and clears the library's device error word on the current device
+ * after synchronising `stream`. *code receives 0 if no bounded wait timed
+ * out, otherwise a nonzero site code; returns BEAM_ERR_DEVICE_TIMEOUT then. */
+beam_status_t beam_get_device_error(int* code, void* stream);
+
+/* Kernel launches issued by the most recent call of each kind on this host
+ * thread's view (a count, for reporting). */
+int beam_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAM_H */

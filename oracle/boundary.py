@@ -16,6 +16,12 @@ Sources:
 Reading taken where the pages are silent: RMSNorm is x / sqrt(mean(x^2) + eps)
 times the weight, the weight applied before the single rounding; exactly three
 rounding points (post-norm output y, new residual h', pre-norm output z).
+
+The residual add is evaluated as (sqrt(n-1) * h + y) / sqrt(n), the same real
+number as sqrt((n-1)/n) * h + y / sqrt(n). In this form float64 is exact
+whenever n-1 is a perfect square (n = 2, 5, 10, 17, ...), where h and y can
+cancel exactly and the result must be exactly 0; for other n the cancellation
+between bf16 inputs is bounded and float64 keeps far more than bf16 precision.
 """
 from __future__ import annotations
 
@@ -29,6 +35,14 @@ def residual_coefficients(n: int):
     if n < 1:
         raise ValueError("boundary index n must be >= 1")
     return np.sqrt((n - 1) / n), 1.0 / np.sqrt(n)
+
+
+def residual(h, y, n: int) -> np.ndarray:
+    """sqrt((n-1)/n) * h + y / sqrt(n), unrounded, as (sqrt(n-1) h + y) / sqrt(n)."""
+    if n < 1:
+        raise ValueError("boundary index n must be >= 1")
+    return (np.sqrt(float(n - 1)) * np.asarray(h, dtype=np.float64) + np.asarray(y, dtype=np.float64)) / np.sqrt(
+        float(n))
 
 
 def rmsnorm(v: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
@@ -45,7 +59,6 @@ def boundary(h, x, w_post, w_pre, n: int, eps: float):
     input and the post-normed sublayer output, each rounded to bf16 once.
     """
     y = round_bf16(rmsnorm(x, w_post, eps))
-    a, b = residual_coefficients(n)
-    h_new = round_bf16(a * np.asarray(h, dtype=np.float64) + b * y)
+    h_new = round_bf16(residual(h, y, n))
     z = round_bf16(rmsnorm(h_new, w_pre, eps))
     return h_new, z, y

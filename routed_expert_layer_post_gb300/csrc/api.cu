@@ -1,0 +1,443 @@
+// C ABI of libbeam.so (declared in include/beam.h): argument validation on
+// the host, workspace carving and stream-ordered launch orchestration. No
+// entry point allocates device memory or synchronises (except the host-buffer
+// layer variant and the device-error query).
+#include "../../include/beam.h"
+#include "kernels.h"
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+namespace beam {
+
+int& launch_counter() {
+  static thread_local int n = 0;
+  return n;
+}
+
+}  // namespace beam
+
+namespace {
+
+using beam::launch_counter;
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+beam_status_t check_config(const beam_moe_config_t* c) {
+  if (c == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (c->hidden <= 0 || c->num_experts <= 0 || c->num_groups <= 0 || c->topk_groups <= 0 || c->topk <= 0 ||
+      c->d_ff <= 0)
+    return BEAM_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.0f) || !std::isfinite(c->eps) || !std::isfinite(c->routed_scale)) return BEAM_ERR_INVALID_ARG;
+  if (c->num_experts % c->num_groups != 0) return BEAM_ERR_INVALID_ARG;
+  if (c->topk_groups > c->num_groups) return BEAM_ERR_INVALID_ARG;
+  if (c->topk > c->topk_groups * (c->num_experts / c->num_groups)) return BEAM_ERR_INVALID_ARG;
+  if (!beam::boundary_supported(c->hidden)) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  if (c->d_ff % 128 != 0) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  if (c->num_experts > 256 || c->num_groups > 32 || c->num_experts / c->num_groups > 32) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  if (c->topk > 16) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  return BEAM_OK;
+}
+
+beam_status_t check_T(int T, const beam_moe_config_t* c) {
+  if (T < 0) return BEAM_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * c->topk >= (1LL << 31)) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  return BEAM_OK;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+beam_status_t device_info(DeviceInfo* out) {
+  static DeviceInfo cache[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return BEAM_ERR_UNSUPPORTED_DEVICE;
+  std::call_once(once[dev], [dev] {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].sms = sms;
+    cache[dev].ok = (major == 10 && minor == 3 && sms > 0);
+  });
+  *out = cache[dev];
+  return out->ok ? BEAM_OK : BEAM_ERR_UNSUPPORTED_DEVICE;
+}
+
+beam_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA; }
+
+// ------------------------------------------------------------------ workspace layouts
+struct ExpertsWs {
+  size_t act, y_perm, gemm, total;
+};
+
+// the SM count enters the split-K plan; size for the largest GB300 part
+constexpr int kPlanSms = 152;
+
+ExpertsWs experts_ws(const beam_moe_config_t* c, int T, int sms) {
+  ExpertsWs w{};
+  const size_t rows = static_cast<size_t>(T) * c->topk;
+  const beam::GemmPlan p0 = beam::plan_gemm(0, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  const beam::GemmPlan p1 = beam::plan_gemm(1, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  w.act = 0;
+  w.y_perm = align_up(w.act + rows * c->d_ff * 2);
+  w.gemm = align_up(w.y_perm + rows * c->hidden * 2);
+  w.total = align_up(w.gemm + beam::gemm_scratch_bytes(p0, p1));
+  return w;
+}
+
+struct LayerWs {
+  size_t z, logits, ids, w, offsets, perm, inv, perm_scratch, x_perm, experts, total;
+};
+
+LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
+  LayerWs l{};
+  const size_t rows = static_cast<size_t>(T) * c->topk;
+  size_t o = 0;
+  l.z = o;            o = align_up(o + static_cast<size_t>(T) * c->hidden * 2);
+  l.logits = o;       o = align_up(o + static_cast<size_t>(T) * c->num_experts * 4);
+  l.ids = o;          o = align_up(o + rows * 4);
+  l.w = o;            o = align_up(o + rows * 4);
+  l.offsets = o;      o = align_up(o + (c->num_experts + 1) * 4);
+  l.perm = o;         o = align_up(o + rows * 4);
+  l.inv = o;          o = align_up(o + rows * 4);
+  l.perm_scratch = o; o = align_up(o + beam::permute_scratch_bytes(T, c->topk, c->num_experts));
+  l.x_perm = o;       o = align_up(o + rows * c->hidden * 2);
+  l.experts = o;      o = align_up(o + experts_ws(c, T, sms).total);
+  l.total = o;
+  return l;
+}
+
+int plan_sms() {
+  DeviceInfo d;
+  if (device_info(&d) == BEAM_OK) return d.sms;
+  return kPlanSms;
+}
+
+void record(const beam_moe_debug_t* dbg, int i, cudaStream_t s) {
+  if (dbg != nullptr && dbg->stage_events[i] != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(dbg->stage_events[i]), s);
+}
+
+beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gu, const uint16_t* w_d,
+                          const float* topk_w, const int32_t* inv, int T, const beam_moe_config_t* c, uint16_t* y,
+                          char* ws, int sms, cudaStream_t s, const beam_moe_debug_t* dbg = nullptr) {
+  const ExpertsWs w = experts_ws(c, T, sms);
+  const int rows = T * c->topk;
+  uint16_t* act = reinterpret_cast<uint16_t*>(ws + w.act);
+  uint16_t* y_perm = reinterpret_cast<uint16_t*>(ws + w.y_perm);
+  void* g = ws + w.gemm;
+  const beam::GemmPlan p0 = beam::plan_gemm(0, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  const beam::GemmPlan p1 = beam::plan_gemm(1, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  // unit counters and split-K tickets start at zero (one memset for both GEMMs)
+  cudaError_t e = beam::clear_gemm_scratch(g, p0, p1, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  record(dbg, 3, s);
+  e = beam::launch_gemm(0, p0, p1, w_gu, x_perm, offsets, rows, c->num_experts, c->hidden, c->d_ff, act, g, sms, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  record(dbg, 4, s);
+  e = beam::launch_gemm(1, p0, p1, w_d, act, offsets, rows, c->num_experts, c->hidden, c->d_ff, y_perm, g, sms, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  record(dbg, 5, s);
+  e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s);
+  record(dbg, 6, s);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* beam_status_string(beam_status_t s) {
+  switch (s) {
+    case BEAM_OK: return "ok";
+    case BEAM_ERR_INVALID_ARG: return "invalid argument";
+    case BEAM_ERR_MISALIGNED: return "misaligned pointer";
+    case BEAM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case BEAM_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case BEAM_ERR_CUDA: return "CUDA error";
+    case BEAM_ERR_DEVICE_TIMEOUT: return "bounded wait timed out on the device";
+    case BEAM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (GB300)";
+  }
+  return "unknown status";
+}
+
+const char* beam_version(void) { return "beam-moe-gb300 0.1 (sm_103a)"; }
+
+int beam_last_launch_count(void) { return launch_counter(); }
+
+beam_status_t beam_boundary_norm(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
+                                 int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out, void* stream) {
+  if (T < 0 || n < 1 || !(eps >= 0.0f) || !std::isfinite(eps)) return BEAM_ERR_INVALID_ARG;
+  if (!beam::boundary_supported(H)) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  launch_counter() = 0;
+  if (T == 0) return BEAM_OK;
+  if (!h || !x || !w_post || !w_pre || !h_out || !z_out) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(x) || !aligned16(w_post) || !aligned16(w_pre) || !aligned16(h_out) ||
+      !aligned16(z_out))
+    return BEAM_ERR_MISALIGNED;
+  if (z_out == h_out || z_out == h || z_out == x || h_out == x) return BEAM_ERR_INVALID_ARG;
+  DeviceInfo d;
+  beam_status_t st = device_info(&d);
+  if (st != BEAM_OK) return st;
+  return cuda_status(
+      beam::launch_boundary(h, x, w_post, w_pre, T, H, eps, n, h_out, z_out, static_cast<cudaStream_t>(stream)));
+}
+
+beam_status_t beam_router_topk(const uint16_t* z, const float* router_w, const float* bias, int T,
+                               const beam_moe_config_t* cfg, float* logits_out, int32_t* topk_ids, float* topk_w,
+                               void* stream) {
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_T(T, cfg)) != BEAM_OK) return st;
+  launch_counter() = 0;
+  if (T == 0) return BEAM_OK;
+  if (!z || !router_w || !bias || !logits_out || !topk_ids || !topk_w) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(z) || !aligned16(router_w) || !aligned4(bias) || !aligned4(logits_out) || !aligned4(topk_ids) ||
+      !aligned4(topk_w))
+    return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = beam::launch_router_logits(z, router_w, T, cfg->hidden, cfg->num_experts, logits_out, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  return cuda_status(beam::launch_topk(logits_out, bias, T, cfg->num_experts, cfg->num_groups, cfg->topk_groups,
+                                       cfg->topk, cfg->routed_scale, topk_ids, topk_w, s));
+}
+
+size_t beam_moe_permute_workspace_size(const beam_moe_config_t* cfg, int T) {
+  if (check_config(cfg) != BEAM_OK || T < 0) return 0;
+  return align_up(beam::permute_scratch_bytes(T, cfg->topk, cfg->num_experts));
+}
+
+beam_status_t beam_moe_permute(const int32_t* topk_ids, const uint16_t* z, int T, const beam_moe_config_t* cfg,
+                               int32_t* expert_offsets, int32_t* perm_token, int32_t* inv_perm, uint16_t* x_perm,
+                               void* ws, size_t ws_bytes, void* stream) {
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_T(T, cfg)) != BEAM_OK) return st;
+  launch_counter() = 0;
+  if (T == 0) return BEAM_OK;
+  if (!topk_ids || !expert_offsets || !perm_token || !inv_perm || !ws) return BEAM_ERR_INVALID_ARG;
+  if (x_perm != nullptr && z == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (!aligned4(topk_ids) || !aligned4(expert_offsets) || !aligned4(perm_token) || !aligned4(inv_perm) ||
+      (x_perm && (!aligned16(x_perm) || !aligned16(z))) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)))
+    return BEAM_ERR_MISALIGNED;
+  if (ws_bytes < beam_moe_permute_workspace_size(cfg, T)) return BEAM_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  return cuda_status(beam::launch_permute(topk_ids, z, T, cfg->topk, cfg->num_experts, cfg->hidden, expert_offsets,
+                                          perm_token, inv_perm, x_perm, ws, static_cast<cudaStream_t>(stream)));
+}
+
+size_t beam_moe_experts_workspace_size(const beam_moe_config_t* cfg, int T) {
+  if (check_config(cfg) != BEAM_OK || T < 0) return 0;
+  return experts_ws(cfg, T, plan_sms()).total;
+}
+
+static beam_status_t check_experts_common(int T, const beam_moe_config_t* cfg, void* ws, size_t ws_bytes) {
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_T(T, cfg)) != BEAM_OK) return st;
+  if (T == 0) return BEAM_OK;
+  if (!ws) return BEAM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return BEAM_ERR_MISALIGNED;
+  if (ws_bytes < beam_moe_experts_workspace_size(cfg, T)) return BEAM_ERR_WORKSPACE_TOO_SMALL;
+  return BEAM_OK;
+}
+
+beam_status_t beam_moe_experts(const uint16_t* x_perm, const int32_t* expert_offsets, const uint16_t* w_gate_up,
+                               const uint16_t* w_down, const float* topk_w, const int32_t* inv_perm, int T,
+                               const beam_moe_config_t* cfg, uint16_t* y_out, void* ws, size_t ws_bytes,
+                               void* stream) {
+  launch_counter() = 0;
+  beam_status_t st = check_experts_common(T, cfg, ws, ws_bytes);
+  if (st != BEAM_OK || T == 0) return st;
+  if (!x_perm || !expert_offsets || !w_gate_up || !w_down || !topk_w || !inv_perm || !y_out)
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y_out) ||
+      !aligned4(expert_offsets) || !aligned4(topk_w) || !aligned4(inv_perm))
+    return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  return run_experts(x_perm, expert_offsets, w_gate_up, w_down, topk_w, inv_perm, T, cfg, y_out,
+                     static_cast<char*>(ws), d.sms, static_cast<cudaStream_t>(stream));
+}
+
+beam_status_t beam_moe_gate_up(const uint16_t* x_perm, const int32_t* expert_offsets, const uint16_t* w_gate_up,
+                               int T, const beam_moe_config_t* cfg, uint16_t* act, void* ws, size_t ws_bytes,
+                               void* stream) {
+  launch_counter() = 0;
+  beam_status_t st = check_experts_common(T, cfg, ws, ws_bytes);
+  if (st != BEAM_OK || T == 0) return st;
+  if (!x_perm || !expert_offsets || !w_gate_up || !act) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate_up) || !aligned16(act) || !aligned4(expert_offsets))
+    return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  const ExpertsWs w = experts_ws(cfg, T, d.sms);
+  const beam::GemmPlan p0 = beam::plan_gemm(0, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  const beam::GemmPlan p1 = beam::plan_gemm(1, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  if (beam::clear_gemm_scratch(static_cast<char*>(ws) + w.gemm, p0, p1, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  return cuda_status(beam::launch_gemm(0, p0, p1, w_gate_up, x_perm, expert_offsets, T * cfg->topk, cfg->num_experts,
+                                       cfg->hidden, cfg->d_ff, act, static_cast<char*>(ws) + w.gemm, d.sms,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+beam_status_t beam_moe_down(const uint16_t* act, const int32_t* expert_offsets, const uint16_t* w_down, int T,
+                            const beam_moe_config_t* cfg, uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  launch_counter() = 0;
+  beam_status_t st = check_experts_common(T, cfg, ws, ws_bytes);
+  if (st != BEAM_OK || T == 0) return st;
+  if (!act || !expert_offsets || !w_down || !y_perm) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(act) || !aligned16(w_down) || !aligned16(y_perm) || !aligned4(expert_offsets))
+    return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  const ExpertsWs w = experts_ws(cfg, T, d.sms);
+  const beam::GemmPlan p0 = beam::plan_gemm(0, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  const beam::GemmPlan p1 = beam::plan_gemm(1, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  if (beam::clear_gemm_scratch(static_cast<char*>(ws) + w.gemm, p0, p1, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  return cuda_status(beam::launch_gemm(1, p0, p1, w_down, act, expert_offsets, T * cfg->topk, cfg->num_experts,
+                                       cfg->hidden, cfg->d_ff, y_perm, static_cast<char*>(ws) + w.gemm, d.sms,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+beam_status_t beam_moe_combine(const uint16_t* y_perm, const float* topk_w, const int32_t* inv_perm, int T,
+                               const beam_moe_config_t* cfg, uint16_t* y_out, void* stream) {
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_T(T, cfg)) != BEAM_OK) return st;
+  launch_counter() = 0;
+  if (T == 0) return BEAM_OK;
+  if (!y_perm || !topk_w || !inv_perm || !y_out) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y_out) || !aligned4(topk_w) || !aligned4(inv_perm))
+    return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  return cuda_status(beam::launch_combine(y_perm, topk_w, inv_perm, T, cfg->topk, cfg->hidden, y_out,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int T) {
+  if (check_config(cfg) != BEAM_OK || T < 0) return 0;
+  return layer_ws(cfg, T, plan_sms()).total;
+}
+
+beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const beam_moe_weights_t* wt, int T,
+                             const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
+                             const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream) {
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_T(T, cfg)) != BEAM_OK) return st;
+  if (n < 1 || wt == nullptr) return BEAM_ERR_INVALID_ARG;
+  launch_counter() = 0;
+  if (T == 0) return BEAM_OK;
+  if (!h || !x || !h_out || !y_out || !ws || !wt->w_post || !wt->w_pre || !wt->router_w || !wt->bias ||
+      !wt->w_gate_up || !wt->w_down)
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(x) || !aligned16(h_out) || !aligned16(y_out) || !aligned16(wt->w_post) ||
+      !aligned16(wt->w_pre) || !aligned16(wt->router_w) || !aligned4(wt->bias) || !aligned16(wt->w_gate_up) ||
+      !aligned16(wt->w_down) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)))
+    return BEAM_ERR_MISALIGNED;
+  if (h_out == x || y_out == h || y_out == x || y_out == h_out) return BEAM_ERR_INVALID_ARG;
+  if (dbg && ((dbg->z && !aligned16(dbg->z)) || (dbg->logits && !aligned4(dbg->logits)) ||
+              (dbg->topk_ids && !aligned4(dbg->topk_ids)) || (dbg->topk_w && !aligned4(dbg->topk_w)) ||
+              (dbg->expert_offsets && !aligned4(dbg->expert_offsets))))
+    return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  if (ws_bytes < layer_ws(cfg, T, d.sms).total) return BEAM_ERR_WORKSPACE_TOO_SMALL;
+  const LayerWs L = layer_ws(cfg, T, d.sms);
+  char* base = static_cast<char*>(ws);
+  uint16_t* z = (dbg && dbg->z) ? dbg->z : reinterpret_cast<uint16_t*>(base + L.z);
+  float* logits = (dbg && dbg->logits) ? dbg->logits : reinterpret_cast<float*>(base + L.logits);
+  int32_t* ids = (dbg && dbg->topk_ids) ? dbg->topk_ids : reinterpret_cast<int32_t*>(base + L.ids);
+  float* w = (dbg && dbg->topk_w) ? dbg->topk_w : reinterpret_cast<float*>(base + L.w);
+  int32_t* offsets = (dbg && dbg->expert_offsets) ? dbg->expert_offsets : reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  int32_t* inv = reinterpret_cast<int32_t*>(base + L.inv);
+  uint16_t* x_perm = reinterpret_cast<uint16_t*>(base + L.x_perm);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int H = cfg->hidden;
+  int launches = 0;
+  record(dbg, 0, s);
+  cudaError_t e = beam::launch_boundary(h, x, wt->w_post, wt->w_pre, T, H, cfg->eps, n, h_out, z, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  record(dbg, 1, s);
+  launches += launch_counter();
+  launch_counter() = 0;
+  e = beam::launch_router_logits(z, wt->router_w, T, H, cfg->num_experts, logits, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  e = beam::launch_topk(logits, wt->bias, T, cfg->num_experts, cfg->num_groups, cfg->topk_groups, cfg->topk,
+                        cfg->routed_scale, ids, w, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  record(dbg, 2, s);
+  e = beam::launch_permute(ids, z, T, cfg->topk, cfg->num_experts, H, offsets, perm, inv, x_perm,
+                           base + L.perm_scratch, s);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  launches += launch_counter();
+  launch_counter() = 0;
+  st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
+                   dbg);
+  launch_counter() += launches;
+  return st;
+}
+
+size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T) {
+  const size_t base = beam_moe_workspace_size(cfg, T);
+  if (base == 0 && T != 0) return 0;
+  const size_t act = align_up(static_cast<size_t>(T) * cfg->hidden * 2);
+  return base + 4 * act;
+}
+
+beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
+                                  const beam_moe_weights_t* wt, int T, const beam_moe_config_t* cfg,
+                                  uint16_t* h_out_host, uint16_t* y_out_host, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_T(T, cfg)) != BEAM_OK) return st;
+  if (n < 1 || wt == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  if (!h_host || !x_host || !h_out_host || !y_out_host || !ws) return BEAM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return BEAM_ERR_MISALIGNED;
+  if (ws_bytes < beam_moe_layer_host_workspace_size(cfg, T)) return BEAM_ERR_WORKSPACE_TOO_SMALL;
+  const size_t bytes = static_cast<size_t>(T) * cfg->hidden * 2;
+  const size_t act = align_up(bytes);
+  char* base = static_cast<char*>(ws);
+  uint16_t* d_h = reinterpret_cast<uint16_t*>(base);
+  uint16_t* d_x = reinterpret_cast<uint16_t*>(base + act);
+  uint16_t* d_hn = reinterpret_cast<uint16_t*>(base + 2 * act);
+  uint16_t* d_y = reinterpret_cast<uint16_t*>(base + 3 * act);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(d_h, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (cudaMemcpyAsync(d_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  st = beam_moe_layer(d_h, d_x, n, wt, T, cfg, d_hn, d_y, nullptr, base + 4 * act, ws_bytes - 4 * act, stream);
+  if (st != BEAM_OK) return st;
+  if (cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (cudaMemcpyAsync(y_out_host, d_y, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+beam_status_t beam_get_device_error(int* code, void* stream) {
+  if (code == nullptr) return BEAM_ERR_INVALID_ARG;
+  *code = 0;
+  if (beam::read_and_clear_device_error(code, static_cast<cudaStream_t>(stream)) != cudaSuccess) return BEAM_ERR_CUDA;
+  return *code != 0 ? BEAM_ERR_DEVICE_TIMEOUT : BEAM_OK;
+}
+
+}  // extern "C"

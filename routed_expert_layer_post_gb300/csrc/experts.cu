@@ -1,0 +1,682 @@
+// Routed SwiGLU experts: two grouped GEMMs on tcgen05 tensor cores fed by
+// TMA, and the deterministic weighted combine.
+//
+// TokenSpeed blog, "TensorRT-LLM NVFP4 MoE": the MoE kernel runs both expert
+// GEMMs, fuses SwiGLU into the first, and computes each token's weighted sum
+// of expert outputs from the FP32 routing weights. vLLM Beam summary, "MoE
+// and residual stream": 256 routed experts, d_ff 2560, no shared expert.
+//
+// Grouped GEMM (one kernel template, two modes):
+//   mode 0 (gate/up): for expert e and a block of 128 intermediate columns f,
+//     D_g = W_g[f-block] . X_e^T and D_u = W_u[f-block] . X_e^T, then
+//     act[row][f] = bf16(silu(D_g) * D_u);
+//   mode 1 (down):    for a block of 128 hidden columns,
+//     D = W_d[h-block] . act_e^T, y_perm[row][h] = bf16(D).
+// The weight block is the MMA's M = 128 operand and the expert's token rows
+// the N operand (16..128): decode batches put 1-3 tokens on an expert, and
+// this orientation keeps the tensor-core tile full of weights instead of
+// padding M with absent tokens. Accumulators live in tensor memory (TMEM),
+// double-buffered so the epilogue of one tile overlaps the MMAs of the next.
+//
+// A persistent CTA per SM walks work units u = blockIdx.x + i * gridDim.x.
+// A unit is (expert, row block, token tile, k-split). Experts' row counts are
+// read from expert_offsets on the device; the host never synchronises. When
+// there are too few tiles to fill the GPU (decode), the reduction dimension
+// is split; partial sums go to the workspace and the last unit of a tile to
+// finish (a ticket counter, no waiting) adds them in fixed split order, so
+// the result does not depend on timing.
+//
+// Warp roles: warp 0 issues TMA loads into a shared-memory ring, warp 1
+// issues tcgen05.mma from one thread, warps 2-5 read TMEM (each warp its
+// 32-lane quarter) and write outputs. Every mbarrier wait is bounded in time;
+// on timeout the CTA records a site code in g_device_error and unwinds.
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+#include <cuda.h>
+#include <cstring>
+#include <mutex>
+
+namespace beam {
+
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;                     // weight rows per tile (MMA M)
+constexpr int kBK = 64;                      // reduction elements per stage: 128 bytes of bf16
+constexpr int kTileABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kMaxE = 256;
+constexpr int kCtrlBytes = 4096;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kDrainNs = 50000000ull;      // 50 ms while unwinding
+constexpr int kQueue = 8;                       // depth of the work-unit queue in shared memory
+
+struct GemmParams {
+  CUtensorMap tmap_w;   // weights, 3-D: (k, row, expert)
+  CUtensorMap tmap_x;   // activations, 2-D: (k, permuted row)
+  const int32_t* offsets;
+  uint16_t* out;
+  float* partials;
+  int* tickets;
+  int* counter;   // dynamic unit counter (zero before the launch)
+  int E;
+  int rows;       // permuted rows (T * K)
+  int n_mb;       // 128-row weight blocks per expert
+  int ksteps;     // reduction length / 64
+  int split;      // split-K factor
+  int out_ld;     // output row length (F for mode 0, H for mode 1)
+  int up_row;     // first up row inside [2F] (mode 0)
+  int max_tiles;  // tiles the workspace was sized for
+};
+
+constexpr int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int MODE, int BN>
+struct Cfg {
+  static constexpr int kNAcc = MODE == 0 ? 2 : 1;
+  static constexpr int kTileBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kNAcc * kTileABytes + kTileBBytes;
+  static constexpr int kStagesRaw = (kSmemLimit - 1024 - kCtrlBytes) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kAccCols = kNAcc * BN;
+  static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
+  static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
+};
+
+// Wait until phase `parity` of `bar` has completed. Gives up after `limit_ns`
+// (or as soon as another role raised the abort flag, if `abort_flag` is set),
+// recording `site` in g_device_error on timeout.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int site,
+                                         uint64_t limit_ns) {
+  const uint32_t addr = ptx::smem_u32(bar);
+  if (ptx::mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(addr, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (ptx::globaltimer() - t0 > limit_ns) {
+        if (abort_flag != nullptr) *abort_flag = 1;
+        atomicCAS(&g_device_error, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void decode_unit(int u, int split, int E, const int* s_tstart, const int* s_ntt, int& e,
+                                            int& mb, int& tt, int& s, int& tile) {
+  tile = u / split;
+  s = u - tile * split;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tstart[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  e = lo;
+  const int local = tile - s_tstart[e];
+  const int ntt = s_ntt[e];
+  mb = local / ntt;
+  tt = local - mb * ntt;
+}
+
+template <int MODE, int BN>
+__device__ __forceinline__ void store_outputs(const GemmParams& p, const float (&v)[2][16], int c0, int valid,
+                                              int row0, int col) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (c0 + j < valid) {
+      const int row = row0 + c0 + j;
+      if (row >= 0 && row < p.rows) {
+        float val;
+        if (MODE == 0) {
+          const float g = v[0][j];
+          val = g / (1.0f + __expf(-g)) * v[1][j];
+        } else {
+          val = v[0][j];
+        }
+        p.out[static_cast<size_t>(row) * p.out_ld + col] = static_cast<uint16_t>(f2bf(val));
+      }
+    }
+  }
+}
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<MODE, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ctrl = tiles + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* qfull = tempty + 2;
+  uint64_t* qempty = qfull + kQueue;
+  uint64_t* drain = qempty + kQueue;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  // [0] abort, [1] last arriver, [2] tile ready, [3] current unit (epilogue broadcast)
+  int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_queue = s_flags + 4;
+  int* s_off = s_queue + kQueue;
+  int* s_ntt = s_off + kMaxE + 1;
+  int* s_tstart = s_ntt + kMaxE;
+  volatile int* abort_flag = s_flags;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 128);
+    }
+    for (int q = 0; q < kQueue; ++q) {
+      ptx::mbar_init(&qfull[q], 1);
+      ptx::mbar_init(&qempty[q], 2);  // released by the MMA thread and the epilogue leader
+    }
+    ptx::mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) s_flags[i] = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&p.tmap_w);
+    ptx::prefetch_tensormap(&p.tmap_x);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
+  __syncthreads();
+  if (warp == 0) {
+    // tiles per expert and their exclusive prefix (lane l owns a contiguous block of experts)
+    const int per_lane = (p.E + 31) / 32;
+    int local = 0;
+    for (int j = 0; j < per_lane; ++j) {
+      const int e = lane * per_lane + j;
+      if (e < p.E) {
+        const int cnt = max(0, s_off[e + 1] - s_off[e]);
+        const int ntt = (cnt + BN - 1) / BN;
+        s_ntt[e] = ntt;
+        local += ntt * p.n_mb;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per_lane; ++j) {
+      const int e = lane * per_lane + j;
+      if (e < p.E) {
+        s_tstart[e] = run;
+        run += s_ntt[e] * p.n_mb;
+      }
+    }
+    if (lane == 31) s_tstart[p.E] = incl;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  int n_tiles = s_tstart[p.E];
+  if (n_tiles > p.max_tiles) {
+    if (tid == 0) atomicCAS(&g_device_error, 0, 100);
+    n_tiles = p.max_tiles;
+  }
+  const int n_units = n_tiles * p.split;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ scheduler + TMA producer
+    // Units are handed out dynamically: the first one is blockIdx.x, the
+    // rest come from a global counter, so SMs that stream faster take more
+    // units and all SMs finish together. Each unit id is published to the
+    // MMA and epilogue warps through a small queue in shared memory.
+    if (lane == 0) {
+      const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
+      const uint64_t pol_x = ptx::policy_evict_last();   // activation tiles are re-read per row block
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int seq = 0;; ++seq) {
+        int u = (seq == 0) ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
+        if (u >= n_units || !ok) u = -1;
+        const int slot = seq % kQueue;
+        if (!wait_bar(&qempty[slot], ((seq / kQueue) & 1) ^ 1u, abort_flag, 5, kTimeoutNs)) {
+          ok = false;
+          u = -1;
+        }
+        s_queue[slot] = u;
+        ptx::mbar_arrive(&qfull[slot]);
+        if (u < 0) break;
+        int e, mb, tt, s, tile;
+        decode_unit(u, p.split, p.E, s_tstart, s_ntt, e, mb, tt, s, tile);
+        const int k0 = s * p.ksteps / p.split, k1 = (s + 1) * p.ksteps / p.split;
+        const int row0 = s_off[e] + tt * BN;
+        for (int k = k0; k < k1; ++k) {
+          if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, 1, kTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = tiles + stage * C::kStageBytes;
+          ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          ptx::tma_load_3d(st, &p.tmap_w, &full[stage], k * kBK, mb * kBM, e, pol_w);
+          if (MODE == 0)
+            ptx::tma_load_3d(st + kTileABytes, &p.tmap_w, &full[stage], k * kBK, p.up_row + mb * kBM, e, pol_w);
+          ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &p.tmap_x, &full[stage], k * kBK, row0, pol_x);
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // unwinding: let the copies already in flight land before the CTA exits
+        for (int i = 0; i < C::kStages && i < issued; ++i) {
+          const uint32_t par = (i < stage) ? phase : (phase ^ 1u);
+          wait_bar(&full[i], par, nullptr, 11, kDrainNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int seq = 0;; ++seq) {
+        const int slot = seq % kQueue;
+        int u = -1;
+        if (wait_bar(&qfull[slot], (seq / kQueue) & 1, abort_flag, 6, kTimeoutNs)) u = s_queue[slot];
+        ptx::mbar_arrive(&qempty[slot]);
+        if (u < 0) break;
+        int e, mb, tt, s, tile;
+        decode_unit(u, p.split, p.E, s_tstart, s_ntt, e, mb, tt, s, tile);
+        const int k0 = s * p.ksteps / p.split, k1 = (s + 1) * p.ksteps / p.split;
+        if (!wait_bar(&tempty[acc], acc_phase ^ 1u, abort_flag, 2, kTimeoutNs)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+        bool ok = true;
+        for (int k = k0; k < k1; ++k) {
+          if (!wait_bar(&full[stage], phase, abort_flag, 3, kTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(tiles + stage * C::kStageBytes);
+          const uint32_t sb = sa + C::kNAcc * kTileABytes;
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j) {
+            const uint64_t bdesc = ptx::smem_desc_k128(sb + j * 32);
+#pragma unroll
+            for (int a = 0; a < C::kNAcc; ++a) {
+              const uint64_t adesc = ptx::smem_desc_k128(sa + a * kTileABytes + j * 32);
+              ptx::mma_bf16(d + a * BN, adesc, bdesc, idesc, (k > k0 || j > 0) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&empty[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // every MMA issued by this thread has completed once `drain` flips
+      ptx::mma_commit(drain);
+      wait_bar(drain, 0, nullptr, 12, kTimeoutNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2-5)
+    const int sub = warp & 3;  // TMEM lane quarter this warp may access
+    const int m = sub * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+    const bool leader = (warp == 2 && lane == 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int seq = 0;; ++seq) {
+      if (leader) {
+        const int slot = seq % kQueue;
+        int u = -1;
+        if (wait_bar(&qfull[slot], (seq / kQueue) & 1, abort_flag, 7, kTimeoutNs)) u = s_queue[slot];
+        ptx::mbar_arrive(&qempty[slot]);
+        int ready = 0;
+        if (u >= 0) ready = wait_bar(&tfull[acc], acc_phase, abort_flag, 4, kTimeoutNs) ? 1 : 0;
+        s_flags[3] = ready ? u : -1;
+      }
+      ptx::named_bar_sync(1, 128);
+      const int u = *reinterpret_cast<volatile int*>(&s_flags[3]);
+      ptx::named_bar_sync(1, 128);
+      if (u < 0) break;
+      ptx::tc_fence_after();
+      int e, mb, tt, s, tile;
+      decode_unit(u, p.split, p.E, s_tstart, s_ntt, e, mb, tt, s, tile);
+      const int row0 = s_off[e] + tt * BN;
+      const int valid = min(BN, s_off[e + 1] - row0);
+      const int col = mb * kBM + m;
+      const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * C::kAccCols);
+      if (p.split == 1) {
+        for (int c0 = 0; c0 < valid; c0 += 16) {
+          uint32_t r[2][16];
+#pragma unroll
+          for (int a = 0; a < C::kNAcc; ++a) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
+          ptx::tmem_ld_wait();
+          float v[2][16];
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[a][j] = a < C::kNAcc ? __uint_as_float(r[a][j]) : 0.f;
+          store_outputs<MODE, BN>(p, v, c0, valid, row0, col);
+        }
+      } else {
+        const size_t slot_elems = static_cast<size_t>(C::kAccCols) * kBM;
+        float* mine = p.partials + (static_cast<size_t>(tile) * p.split + s) * slot_elems;
+        for (int c0 = 0; c0 < valid; c0 += 16) {
+          uint32_t r[2][16];
+#pragma unroll
+          for (int a = 0; a < C::kNAcc; ++a) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int a = 0; a < C::kNAcc; ++a)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < valid) mine[static_cast<size_t>(a * BN + c0 + j) * kBM + m] = __uint_as_float(r[a][j]);
+        }
+        __threadfence();
+        ptx::named_bar_sync(1, 128);
+        if (leader) s_flags[1] = (atomicAdd(&p.tickets[tile], 1) == p.split - 1) ? 1 : 0;
+        ptx::named_bar_sync(1, 128);
+        const int last = *reinterpret_cast<volatile int*>(&s_flags[1]);
+        if (last) {
+          __threadfence();
+          const float* tile_parts = p.partials + static_cast<size_t>(tile) * p.split * slot_elems;
+          for (int c0 = 0; c0 < valid; c0 += 16) {
+            uint32_t r[2][16];
+#pragma unroll
+            for (int a = 0; a < C::kNAcc; ++a) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
+            ptx::tmem_ld_wait();
+            float v[2][16];
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float sum = 0.f;
+                if (a < C::kNAcc && c0 + j < valid) {
+                  const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
+                  for (int ss = 0; ss < p.split; ++ss) {
+                    const float x = (ss == s) ? __uint_as_float(r[a][j]) : __ldcg(tile_parts + ss * slot_elems + off);
+                    sum = (ss == 0) ? x : sum + x;
+                  }
+                }
+                v[a][j] = sum;
+              }
+            }
+            store_outputs<MODE, BN>(p, v, c0, valid, row0, col);
+          }
+          if (leader) p.tickets[tile] = 0;
+        }
+        ptx::named_bar_sync(1, 128);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// y[t] = bf16(sum_k w[t][k] * y_perm[inv_perm[t*K+k]]), k in slot order, one
+// thread per 8 hidden columns of a token; no atomics.
+constexpr int kMaxTopK = 16;
+
+__global__ void __launch_bounds__(256)
+    combine_kernel(const uint4* __restrict__ y_perm, const float* __restrict__ w, const int32_t* __restrict__ inv,
+                   int T, int K, int chunks, uint4* __restrict__ y) {
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<size_t>(T) * chunks) return;
+  const int t = static_cast<int>(idx / chunks);
+  const int c = static_cast<int>(idx - static_cast<size_t>(t) * chunks);
+  // all K rows are requested before the first one is used
+  uint4 rows[kMaxTopK];
+  float wk[kMaxTopK];
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    rows[k] = make_uint4(0u, 0u, 0u, 0u);
+    wk[k] = 0.f;
+    if (k < K) {
+      const int p = inv[static_cast<size_t>(t) * K + k];
+      if (p >= 0) {
+        wk[k] = w[static_cast<size_t>(t) * K + k];
+        rows[k] = y_perm[static_cast<size_t>(p) * chunks + c];
+      }
+    }
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    if (k < K) {
+      float f[8];
+      unpack8(rows[k], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[k], f[i], acc[i]);
+    }
+  }
+  y[idx] = pack8(acc);
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeFn = decltype(&cuTensorMapEncodeTiled);
+
+EncodeFn get_encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+
+bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                const cuuint32_t* box) {
+  EncodeFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, int BN>
+cudaError_t launch_mode_bn(const GemmParams& prm, int grid, cudaStream_t stream) {
+  using C = Cfg<MODE, BN>;
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  moe_gemm_kernel<MODE, BN><<<grid, kThreads, C::kSmemBytes, stream>>>(prm);
+  ++launch_counter();
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t stream) {
+  switch (bn) {
+    case 16: return launch_mode_bn<MODE, 16>(prm, grid, stream);
+    case 32: return launch_mode_bn<MODE, 32>(prm, grid, stream);
+    case 64: return launch_mode_bn<MODE, 64>(prm, grid, stream);
+    default: return launch_mode_bn<MODE, 128>(prm, grid, stream);
+  }
+}
+
+int accum_cols(int mode, int bn) { return (mode == 0 ? 2 : 1) * bn; }
+
+}  // namespace
+
+GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms) {
+  GemmPlan plan{};
+  const long long entries = static_cast<long long>(T) * K;
+  const long long touched = entries < E ? entries : E;
+  const double r = touched > 0 ? static_cast<double>(entries) / static_cast<double>(touched) : 1.0;
+  int bn = 16;
+  while (bn < 128 && 1.25 * r > bn) bn <<= 1;
+  const int n_mb = mode == 0 ? F / kBM : H / kBM;
+  const int ksteps = mode == 0 ? H / kBK : F / kBK;
+  plan.bn = bn;
+  plan.max_tiles = static_cast<int>((touched + entries / bn) * n_mb);
+  const long long per_expert = static_cast<long long>((r + bn - 1) / bn);
+  const long long est = touched * (per_expert > 0 ? per_expert : 1) * n_mb;
+  int split = 1;
+  if (est < 4LL * num_sms) {
+    double best = 0.0;
+    for (int s = 1; s <= ksteps; ++s) {
+      if (ksteps % s != 0 || ksteps / s < 4) continue;
+      const long long units = est * s;
+      const long long waves = (units + num_sms - 1) / num_sms;
+      const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
+      if (eff > best + 1e-9) {
+        best = eff;
+        split = s;
+      }
+      if (eff >= 0.95) break;
+    }
+  }
+  plan.split = split;
+  return plan;
+}
+
+namespace {
+
+// Scratch shared by the gate/up and down GEMMs of one experts pass:
+//   [0, 256)                     two dynamic unit counters (one per GEMM)
+//   [256, 256 + tickets)         split-K tickets, sized for the larger plan
+//   [.., ..)                     split-K partial sums, sized for the larger plan
+constexpr size_t kCounterBytes = 256;
+
+size_t ticket_bytes(const GemmPlan& g, const GemmPlan& d) {
+  const int cap = g.max_tiles > d.max_tiles ? g.max_tiles : d.max_tiles;
+  return (static_cast<size_t>(cap) * sizeof(int) + 255) & ~static_cast<size_t>(255);
+}
+
+size_t partial_bytes(int mode, const GemmPlan& plan) {
+  if (plan.split <= 1) return 0;
+  return static_cast<size_t>(plan.max_tiles) * plan.split * accum_cols(mode, plan.bn) * kBM * sizeof(float);
+}
+
+}  // namespace
+
+size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down) {
+  const size_t a = partial_bytes(0, gate_up), b = partial_bytes(1, down);
+  return kCounterBytes + ticket_bytes(gate_up, down) + (a > b ? a : b);
+}
+
+cudaError_t clear_gemm_scratch(void* scratch, const GemmPlan& gate_up, const GemmPlan& down, cudaStream_t stream) {
+  return cudaMemsetAsync(scratch, 0, kCounterBytes + ticket_bytes(gate_up, down), stream);
+}
+
+cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
+                        const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
+                        void* scratch, int num_sms, cudaStream_t stream) {
+  const GemmPlan& plan = mode == 0 ? gate_up : down;
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int kdim = mode == 0 ? H : F;    // reduction length
+  const int wrows = mode == 0 ? 2 * F : H;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(wrows),
+                                static_cast<cuuint64_t>(E)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kdim) * 2,
+                                   static_cast<cuuint64_t>(kdim) * 2 * static_cast<cuuint64_t>(wrows)};
+    const cuuint32_t box[3] = {kBK, kBM, 1};
+    if (!encode_map(&prm.tmap_w, weights, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim) * 2};
+    const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(plan.bn)};
+    if (!encode_map(&prm.tmap_x, act_in, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  char* base = static_cast<char*>(scratch);
+  prm.counter = reinterpret_cast<int*>(base) + mode;
+  prm.tickets = reinterpret_cast<int*>(base + kCounterBytes);
+  prm.partials =
+      plan.split > 1 ? reinterpret_cast<float*>(base + kCounterBytes + ticket_bytes(gate_up, down)) : nullptr;
+  prm.offsets = offsets;
+  prm.out = out;
+  prm.E = E;
+  prm.rows = rows;
+  prm.n_mb = mode == 0 ? F / kBM : H / kBM;
+  prm.ksteps = kdim / kBK;
+  prm.split = plan.split;
+  prm.out_ld = mode == 0 ? F : H;
+  prm.up_row = F;
+  prm.max_tiles = plan.max_tiles;
+  return mode == 0 ? launch_mode<0>(plan.bn, prm, num_sms, stream) : launch_mode<1>(plan.bn, prm, num_sms, stream);
+}
+
+cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,
+                           uint16_t* y, cudaStream_t stream) {
+  const int chunks = H / 8;
+  const size_t n = static_cast<size_t>(T) * chunks;
+  const int blocks = static_cast<int>((n + 255) / 256);
+  combine_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(y_perm), w, inv_perm, T, K, chunks,
+                                             reinterpret_cast<uint4*>(y));
+  ++launch_counter();
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream) {
+  cudaError_t err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return err;
+  int v = 0;
+  err = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+  if (err != cudaSuccess) return err;
+  if (v != 0) {
+    const int zero = 0;
+    err = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+  }
+  *code = v;
+  return err;
+}
+
+}  // namespace beam

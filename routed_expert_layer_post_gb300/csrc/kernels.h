@@ -1,0 +1,54 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation
+// units. Plain pointers and sizes; every launcher enqueues on `stream` and
+// returns the launch status.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace beam {
+
+// Number of kernel launches issued by the calling host thread since the
+// counter was last reset (for reporting).
+int& launch_counter();
+
+// ---- boundary (boundary.cu)
+// n >= 1 is the index of the residual add (coefficients sqrt((n-1)/n), 1/sqrt(n))
+cudaError_t launch_boundary(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
+                            int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out, cudaStream_t stream);
+bool boundary_supported(int H);
+
+// ---- router (router.cu)
+cudaError_t launch_router_logits(const uint16_t* z, const float* W, int T, int H, int E, float* logits,
+                                 cudaStream_t stream);
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int G, int TG, int K, float scale,
+                        int32_t* ids, float* w, cudaStream_t stream);
+
+// ---- permutation (permute.cu)
+size_t permute_scratch_bytes(int T, int K, int E);
+cudaError_t launch_permute(const int32_t* ids, const uint16_t* z, int T, int K, int E, int H, int32_t* offsets,
+                           int32_t* perm_token, int32_t* inv_perm, uint16_t* x_perm, void* scratch,
+                           cudaStream_t stream);
+
+// ---- experts (experts.cu)
+struct GemmPlan {
+  int bn;         // token tile (MMA N): 16, 32, 64 or 128
+  int split;      // split-K factor (1 = no partial sums)
+  int max_tiles;  // upper bound on (expert, row-block, token-tile) tiles
+};
+// mode 0: gate/up + SwiGLU (weight rows 2F, reduction H); mode 1: down (rows H, reduction F)
+GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms);
+// Scratch shared by one gate/up + down pass (unit counters, split-K tickets
+// and partial sums); it must be cleared with clear_gemm_scratch before the
+// gate/up GEMM (one memset; each GEMM leaves its tickets at zero).
+size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down);
+cudaError_t clear_gemm_scratch(void* scratch, const GemmPlan& gate_up, const GemmPlan& down, cudaStream_t stream);
+cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
+                        const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
+                        void* scratch, int num_sms, cudaStream_t stream);
+cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,
+                           uint16_t* y, cudaStream_t stream);
+cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream);
+
+}  // namespace beam

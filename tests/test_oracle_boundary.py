@@ -6,7 +6,7 @@ import numpy as np
 import torch
 
 from oracle import bf16
-from oracle.boundary import boundary, residual_coefficients, rmsnorm
+from oracle.boundary import boundary, residual, residual_coefficients, rmsnorm
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -83,3 +83,24 @@ def test_outputs_are_bf16_values():
     w = bf16.round_bf16(1 + 0.02 * rng.standard_normal(256))
     for arr in boundary(h, x, w, w, 7, 1e-6):
         assert np.array_equal(bf16.round_bf16(arr), arr)
+
+
+def test_residual_form_equals_the_pages_formula():
+    rng = np.random.default_rng(6)
+    h = bf16.round_bf16(rng.standard_normal(10000))
+    y = bf16.round_bf16(rng.standard_normal(10000))
+    for n in (1, 2, 3, 10, 20, 60, 100):
+        a, b = residual_coefficients(n)
+        np.testing.assert_allclose(residual(h, y, n), a * h + b * y, rtol=1e-12, atol=1e-15)
+
+
+def test_exact_cancellation_gives_zero():
+    # n - 1 a perfect square: sqrt((n-1)/n) h + y / sqrt(n) = 0 exactly when y = -sqrt(n-1) h
+    h = np.array([1.0, -0.75, 3.0, 2.0 ** -20])
+    for n, m in ((2, 1.0), (5, 2.0), (10, 3.0), (17, 4.0)):
+        y = -m * h
+        assert np.all(residual(h, y, n) == 0.0)
+    # through the whole boundary: x = (-3, -3) normalises to y = -1, h = 1/3 would
+    # not be bf16, so take h = 1 with n = 2 (y = -h)
+    h_new, _, _ = boundary(np.ones((1, 2)), -np.ones((1, 2)), np.ones(2), np.ones(2), 2, 0.0)
+    assert np.all(h_new == 0.0)
