@@ -140,6 +140,25 @@ beam_status_t beam_moe_permute(const int32_t* topk_ids, const uint16_t* z, int T
                                int32_t* perm_token, int32_t* inv_perm, uint16_t* x_perm, void* ws,
                                size_t ws_bytes, void* stream);
 
+/* beam_moe_permute for callers that cannot provide a workspace (the pages
+ * have no counterpart; this is a convenience of this library). Some callers
+ * have no way to hand the library scratch memory -- for example an operator
+ * plugin that only receives the tensors it declares, or a latency-critical
+ * loop where a device allocation is not allowed. This variant runs the same
+ * kernels as beam_moe_permute with its scratch in a fixed array inside the
+ * library's device memory (131,328 bytes per GPU, held until the process
+ * exits), so it takes no workspace and allocates nothing. Arguments and
+ * outputs are those of beam_moe_permute. Limits: T * K <= BEAM_NO_ALLOC_MAX_PAIRS
+ * and E <= 256, else BEAM_ERR_WORKSPACE_TOO_SMALL. All calls on a device share
+ * the array: calls whose kernels may overlap on the GPU (unordered streams)
+ * race and must not be issued. The first call on each device looks up the
+ * array's device address; make it before any stream capture on that device. */
+#define BEAM_NO_ALLOC_MAX_PAIRS 131072
+beam_status_t beam_moe_permute_no_alloc(const int32_t* topk_ids, const uint16_t* z, int T,
+                                        const beam_moe_config_t* cfg, int32_t* expert_offsets,
+                                        int32_t* perm_token, int32_t* inv_perm, uint16_t* x_perm,
+                                        void* stream);
+
 /* Routed SwiGLU experts and weighted combine (TokenSpeed blog, "TensorRT-LLM
  * NVFP4 MoE": both expert GEMMs, SwiGLU fused into the first, weighted sum of
  * expert outputs per token; vLLM Beam summary: 256 experts, d_ff 2560):

@@ -86,6 +86,8 @@ _SIGNATURES = {
                                     ctypes.POINTER(MoeConfig), c_void_p, c_void_p, c_void_p, c_size_t,
                                     c_void_p]),
     "beam_get_device_error": (c_int, [ctypes.POINTER(c_int), c_void_p]),
+    "beam_moe_permute_no_alloc": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeConfig), c_void_p,
+                                          c_void_p, c_void_p, c_void_p, c_void_p]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
