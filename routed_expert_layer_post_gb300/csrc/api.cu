@@ -97,7 +97,7 @@ ExpertsWs experts_ws(const beam_moe_config_t* c, int T, int sms) {
 }
 
 struct LayerWs {
-  size_t z, logits, ids, w, offsets, perm, inv, perm_scratch, x_perm, experts, total;
+  size_t z, logits, ids, w, offsets, perm, inv, perm_scratch, router_ticket, x_perm, experts, total;
 };
 
 LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
@@ -112,6 +112,7 @@ LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
   l.perm = o;         o = align_up(o + rows * 4);
   l.inv = o;          o = align_up(o + rows * 4);
   l.perm_scratch = o; o = align_up(o + beam::permute_scratch_bytes(T, c->topk, c->num_experts));
+  l.router_ticket = o; o = align_up(o + sizeof(int));
   l.x_perm = o;       o = align_up(o + rows * c->hidden * 2);
   l.experts = o;      o = align_up(o + experts_ws(c, T, sms).total);
   l.total = o;
@@ -128,9 +129,13 @@ void record(const beam_moe_debug_t* dbg, int i, cudaStream_t s) {
   if (dbg != nullptr && dbg->stage_events[i] != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(dbg->stage_events[i]), s);
 }
 
+// Gate/up GEMM -> down GEMM -> combine. `pdl`: launch with programmatic
+// dependent launch; `cleared`: the GEMM counters and tickets were already
+// zeroed by an earlier kernel (the layer's permutation does it).
 beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gu, const uint16_t* w_d,
                           const float* topk_w, const int32_t* inv, int T, const beam_moe_config_t* c, uint16_t* y,
-                          char* ws, int sms, cudaStream_t s, const beam_moe_debug_t* dbg = nullptr) {
+                          char* ws, int sms, cudaStream_t s, const beam_moe_debug_t* dbg = nullptr, bool pdl = false,
+                          bool cleared = false) {
   const ExpertsWs w = experts_ws(c, T, sms);
   const int rows = T * c->topk;
   uint16_t* act = reinterpret_cast<uint16_t*>(ws + w.act);
@@ -139,16 +144,18 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
   const beam::GemmPlan p0 = beam::plan_gemm(0, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
   const beam::GemmPlan p1 = beam::plan_gemm(1, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
   // unit counters and split-K tickets start at zero (one memset for both GEMMs)
-  cudaError_t e = beam::clear_gemm_scratch(g, p0, p1, s);
-  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!cleared && (e = beam::clear_gemm_scratch(g, p0, p1, s)) != cudaSuccess) return BEAM_ERR_CUDA;
   record(dbg, 3, s);
-  e = beam::launch_gemm(0, p0, p1, w_gu, x_perm, offsets, rows, c->num_experts, c->hidden, c->d_ff, act, g, sms, s);
+  e = beam::launch_gemm(0, p0, p1, w_gu, x_perm, offsets, rows, c->num_experts, c->hidden, c->d_ff, act, g, sms, s,
+                        pdl);
   if (e != cudaSuccess) return BEAM_ERR_CUDA;
   record(dbg, 4, s);
-  e = beam::launch_gemm(1, p0, p1, w_d, act, offsets, rows, c->num_experts, c->hidden, c->d_ff, y_perm, g, sms, s);
+  e = beam::launch_gemm(1, p0, p1, w_d, act, offsets, rows, c->num_experts, c->hidden, c->d_ff, y_perm, g, sms, s,
+                        pdl);
   if (e != cudaSuccess) return BEAM_ERR_CUDA;
   record(dbg, 5, s);
-  e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s);
+  e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, pdl);
   record(dbg, 6, s);
   return cuda_status(e);
 }
@@ -375,24 +382,40 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
   const int H = cfg->hidden;
   int launches = 0;
   record(dbg, 0, s);
-  cudaError_t e = beam::launch_boundary(h, x, wt->w_post, wt->w_pre, T, H, cfg->eps, n, h_out, z, s);
+  // every kernel of the layer is launched with programmatic dependent launch
+  const bool pdl = true;
+  // the boundary also zeroes the router's ticket (used when router and top-k share a launch)
+  int* router_ticket = reinterpret_cast<int*>(base + L.router_ticket);
+  cudaError_t e =
+      beam::launch_boundary(h, x, wt->w_post, wt->w_pre, T, H, cfg->eps, n, h_out, z, s, pdl, router_ticket);
   if (e != cudaSuccess) return BEAM_ERR_CUDA;
   record(dbg, 1, s);
   launches += launch_counter();
   launch_counter() = 0;
-  e = beam::launch_router_logits(z, wt->router_w, T, H, cfg->num_experts, logits, s);
-  if (e != cudaSuccess) return BEAM_ERR_CUDA;
-  e = beam::launch_topk(logits, wt->bias, T, cfg->num_experts, cfg->num_groups, cfg->topk_groups, cfg->topk,
-                        cfg->routed_scale, ids, w, s);
-  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  if (beam::router_topk_fusable(T, cfg->num_experts, cfg->num_groups)) {
+    e = beam::launch_router_topk_fused(z, wt->router_w, wt->bias, T, H, cfg->num_experts, cfg->num_groups,
+                                       cfg->topk_groups, cfg->topk, cfg->routed_scale, logits, ids, w,
+                                       router_ticket, s, pdl);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  } else {
+    e = beam::launch_router_logits(z, wt->router_w, T, H, cfg->num_experts, logits, s, pdl);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    e = beam::launch_topk(logits, wt->bias, T, cfg->num_experts, cfg->num_groups, cfg->topk_groups, cfg->topk,
+                          cfg->routed_scale, ids, w, s, pdl);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
   record(dbg, 2, s);
+  // the permutation also zeroes the experts' counters and tickets
+  const beam::GemmPlan p0 = beam::plan_gemm(0, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  const beam::GemmPlan p1 = beam::plan_gemm(1, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  char* gemm_scratch = base + L.experts + experts_ws(cfg, T, d.sms).gemm;
   e = beam::launch_permute(ids, z, T, cfg->topk, cfg->num_experts, H, offsets, perm, inv, x_perm,
-                           base + L.perm_scratch, s);
+                           base + L.perm_scratch, s, pdl, gemm_scratch, beam::gemm_clear_bytes(p0, p1));
   if (e != cudaSuccess) return BEAM_ERR_CUDA;
   launches += launch_counter();
   launch_counter() = 0;
   st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
-                   dbg);
+                   dbg, pdl, /*cleared=*/true);
   launch_counter() += launches;
   return st;
 }

@@ -54,6 +54,7 @@ constexpr int kSmemLimit = 227 * 1024;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainNs = 50000000ull;      // 50 ms while unwinding
 constexpr int kQueue = 8;                       // depth of the work-unit queue in shared memory
+constexpr int kMaxSplit = 20;                   // largest split-K factor (partials summed from registers)
 
 struct GemmParams {
   CUtensorMap tmap_w;   // weights, 3-D: (k, row, expert)
@@ -200,6 +201,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     ptx::tmem_alloc(tmem_slot, C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  // Programmatic dependent launch: everything above overlaps the previous
+  // kernel. The gate/up GEMM reads that kernel's outputs (offsets, x_perm)
+  // and waits here. The down GEMM's offsets and weights come from earlier
+  // kernels (its predecessor only waits for them), so it builds its tile
+  // table and streams weight tiles now; only its activation loads and its
+  // epilogue wait for the gate/up GEMM.
+  if (MODE == 0) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+  }
   for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
   __syncthreads();
   if (warp == 0) {
@@ -255,9 +266,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
+      // mode 1: activation (B) loads wait for the previous kernel; until then
+      // stages get their weight tile only and are remembered here
+      bool dep_ready = (MODE == 0);
+      int npend = 0;
+      int pend_stage[C::kStages], pend_k[C::kStages], pend_row[C::kStages];
+      auto release_pending = [&]() {
+        ptx::griddep_wait();
+        ptx::griddep_launch_dependents();
+        for (int i = 0; i < npend; ++i)
+          ptx::tma_load_2d(tiles + pend_stage[i] * C::kStageBytes + C::kNAcc * kTileABytes, &p.tmap_x,
+                           &full[pend_stage[i]], pend_k[i] * kBK, pend_row[i], pol_x);
+        npend = 0;
+        dep_ready = true;
+      };
+      int u_next = static_cast<int>(blockIdx.x);
       for (int seq = 0;; ++seq) {
-        int u = (seq == 0) ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
+        int u = u_next;
         if (u >= n_units || !ok) u = -1;
+        if (u < 0 && !dep_ready) release_pending();
         const int slot = seq % kQueue;
         if (!wait_bar(&qempty[slot], ((seq / kQueue) & 1) ^ 1u, abort_flag, 5, kTimeoutNs)) {
           ok = false;
@@ -266,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         s_queue[slot] = u;
         ptx::mbar_arrive(&qfull[slot]);
         if (u < 0) break;
+        // ask for the following unit now: the atomic's round trip overlaps this unit's loads
+        u_next = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
         int e, mb, tt, s, tile;
         decode_unit(u, p.split, p.E, s_tstart, s_ntt, e, mb, tt, s, tile);
         const int k0 = s * p.ksteps / p.split, k1 = (s + 1) * p.ksteps / p.split;
@@ -280,7 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           ptx::tma_load_3d(st, &p.tmap_w, &full[stage], k * kBK, mb * kBM, e, pol_w);
           if (MODE == 0)
             ptx::tma_load_3d(st + kTileABytes, &p.tmap_w, &full[stage], k * kBK, p.up_row + mb * kBM, e, pol_w);
-          ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &p.tmap_x, &full[stage], k * kBK, row0, pol_x);
+          if (dep_ready) {
+            ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &p.tmap_x, &full[stage], k * kBK, row0, pol_x);
+          } else {
+            pend_stage[npend] = stage;
+            pend_k[npend] = k;
+            pend_row[npend] = row0;
+            if (++npend == C::kStages) release_pending();  // the ring is full: the MMA needs these tiles
+          }
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -355,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     const int m = sub * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
     const bool leader = (warp == 2 && lane == 0);
+    if (MODE == 1) ptx::griddep_wait();  // tickets and partial sums were last used by the previous kernel
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int seq = 0;; ++seq) {
@@ -405,13 +442,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             for (int j = 0; j < 16; ++j)
               if (c0 + j < valid) mine[static_cast<size_t>(a * BN + c0 + j) * kBM + m] = __uint_as_float(r[a][j]);
         }
-        __threadfence();
+        // the barrier orders every thread's partial stores before the
+        // leader's fence; the fence (cumulative) then publishes them before
+        // the ticket, and on the reading side orders the ticket before the
+        // partial loads that follow the second barrier
         ptx::named_bar_sync(1, 128);
-        if (leader) s_flags[1] = (atomicAdd(&p.tickets[tile], 1) == p.split - 1) ? 1 : 0;
+        if (leader) {
+          __threadfence();
+          const int last_now = (atomicAdd(&p.tickets[tile], 1) == p.split - 1) ? 1 : 0;
+          if (last_now) __threadfence();
+          s_flags[1] = last_now;
+        }
         ptx::named_bar_sync(1, 128);
         const int last = *reinterpret_cast<volatile int*>(&s_flags[1]);
         if (last) {
-          __threadfence();
           const float* tile_parts = p.partials + static_cast<size_t>(tile) * p.split * slot_elems;
           for (int c0 = 0; c0 < valid; c0 += 16) {
             uint32_t r[2][16];
@@ -420,18 +464,37 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             ptx::tmem_ld_wait();
             float v[2][16];
 #pragma unroll
-            for (int a = 0; a < 2; ++a) {
+            for (int a = 0; a < 2; ++a)
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
+              for (int j = 0; j < 16; ++j) v[a][j] = 0.f;
+            for (int j = 0; j < 16 && c0 + j < valid; ++j) {
+              // all partials of this column are requested before any is added,
+              // then summed in split order (the result does not depend on timing)
+              float x[C::kNAcc][kMaxSplit];
+#pragma unroll
+              for (int a = 0; a < C::kNAcc; ++a) {
+                const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
+#pragma unroll
+                for (int ss = 0; ss < kMaxSplit; ++ss)
+                  x[a][ss] = (ss < p.split && ss != s) ? __ldcg(tile_parts + ss * slot_elems + off) : 0.f;
+              }
+#pragma unroll
+              for (int a = 0; a < C::kNAcc; ++a) {
+                float mine_v = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                  if (jj == j) mine_v = __uint_as_float(r[a][jj]);
                 float sum = 0.f;
-                if (a < C::kNAcc && c0 + j < valid) {
-                  const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
-                  for (int ss = 0; ss < p.split; ++ss) {
-                    const float x = (ss == s) ? __uint_as_float(r[a][j]) : __ldcg(tile_parts + ss * slot_elems + off);
-                    sum = (ss == 0) ? x : sum + x;
+#pragma unroll
+                for (int ss = 0; ss < kMaxSplit; ++ss) {
+                  if (ss < p.split) {
+                    const float xv = (ss == s) ? mine_v : x[a][ss];
+                    sum = (ss == 0) ? xv : sum + xv;
                   }
                 }
-                v[a][j] = sum;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                  if (jj == j) v[a][jj] = sum;
               }
             }
             store_outputs<MODE, BN>(p, v, c0, valid, row0, col);
@@ -463,6 +526,8 @@ constexpr int kMaxTopK = 16;
 __global__ void __launch_bounds__(256)
     combine_kernel(const uint4* __restrict__ y_perm, const float* __restrict__ w, const int32_t* __restrict__ inv,
                    int T, int K, int chunks, uint4* __restrict__ y) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<size_t>(T) * chunks) return;
   const int t = static_cast<int>(idx / chunks);
@@ -523,7 +588,7 @@ bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* 
 }
 
 template <int MODE, int BN>
-cudaError_t launch_mode_bn(const GemmParams& prm, int grid, cudaStream_t stream) {
+cudaError_t launch_mode_bn(const GemmParams& prm, int grid, cudaStream_t stream, bool pdl) {
   using C = Cfg<MODE, BN>;
   static std::once_flag once[64];
   int dev = 0;
@@ -534,18 +599,19 @@ cudaError_t launch_mode_bn(const GemmParams& prm, int grid, cudaStream_t stream)
                                     C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  moe_gemm_kernel<MODE, BN><<<grid, kThreads, C::kSmemBytes, stream>>>(prm);
+  const cudaError_t err =
+      launch_kernel(moe_gemm_kernel<MODE, BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, prm);
   ++launch_counter();
-  return cudaGetLastError();
+  return err;
 }
 
 template <int MODE>
-cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t stream) {
+cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t stream, bool pdl) {
   switch (bn) {
-    case 16: return launch_mode_bn<MODE, 16>(prm, grid, stream);
-    case 32: return launch_mode_bn<MODE, 32>(prm, grid, stream);
-    case 64: return launch_mode_bn<MODE, 64>(prm, grid, stream);
-    default: return launch_mode_bn<MODE, 128>(prm, grid, stream);
+    case 16: return launch_mode_bn<MODE, 16>(prm, grid, stream, pdl);
+    case 32: return launch_mode_bn<MODE, 32>(prm, grid, stream, pdl);
+    case 64: return launch_mode_bn<MODE, 64>(prm, grid, stream, pdl);
+    default: return launch_mode_bn<MODE, 128>(prm, grid, stream, pdl);
   }
 }
 
@@ -566,19 +632,19 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms) {
   plan.max_tiles = static_cast<int>((touched + entries / bn) * n_mb);
   const long long per_expert = static_cast<long long>((r + bn - 1) / bn);
   const long long est = touched * (per_expert > 0 ? per_expert : 1) * n_mb;
+  // Units are handed out dynamically, so balance depends on how small the
+  // last units are: when tiles are few (decode), split the reduction until
+  // there are at least 16 units per SM, keeping at least 128 KB of weights
+  // per unit (4 k-steps of gate+up rows, 8 of down rows) so that the
+  // per-unit epilogue stays hidden behind the next unit's loads.
+  const int min_ksteps = mode == 0 ? 4 : 8;
   int split = 1;
-  if (est < 4LL * num_sms) {
-    double best = 0.0;
-    for (int s = 1; s <= ksteps; ++s) {
-      if (ksteps % s != 0 || ksteps / s < 4) continue;
-      const long long units = est * s;
-      const long long waves = (units + num_sms - 1) / num_sms;
-      const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
-      if (eff > best + 1e-9) {
-        best = eff;
-        split = s;
-      }
-      if (eff >= 0.95) break;
+  if (est < 16LL * num_sms) {
+    for (int s = 2; s <= ksteps && s <= kMaxSplit; ++s) {
+      if (ksteps % s != 0) continue;
+      if (ksteps / s < min_ksteps) break;
+      split = s;
+      if (est * s >= 16LL * num_sms) break;
     }
   }
   plan.split = split;
@@ -610,13 +676,17 @@ size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down) {
   return kCounterBytes + ticket_bytes(gate_up, down) + (a > b ? a : b);
 }
 
+size_t gemm_clear_bytes(const GemmPlan& gate_up, const GemmPlan& down) {
+  return kCounterBytes + ticket_bytes(gate_up, down);
+}
+
 cudaError_t clear_gemm_scratch(void* scratch, const GemmPlan& gate_up, const GemmPlan& down, cudaStream_t stream) {
-  return cudaMemsetAsync(scratch, 0, kCounterBytes + ticket_bytes(gate_up, down), stream);
+  return cudaMemsetAsync(scratch, 0, gemm_clear_bytes(gate_up, down), stream);
 }
 
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
-                        void* scratch, int num_sms, cudaStream_t stream) {
+                        void* scratch, int num_sms, cudaStream_t stream, bool pdl) {
   const GemmPlan& plan = mode == 0 ? gate_up : down;
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -651,18 +721,20 @@ cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down,
   prm.out_ld = mode == 0 ? F : H;
   prm.up_row = F;
   prm.max_tiles = plan.max_tiles;
-  return mode == 0 ? launch_mode<0>(plan.bn, prm, num_sms, stream) : launch_mode<1>(plan.bn, prm, num_sms, stream);
+  return mode == 0 ? launch_mode<0>(plan.bn, prm, num_sms, stream, pdl)
+                   : launch_mode<1>(plan.bn, prm, num_sms, stream, pdl);
 }
 
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,
-                           uint16_t* y, cudaStream_t stream) {
+                           uint16_t* y, cudaStream_t stream, bool pdl) {
   const int chunks = H / 8;
   const size_t n = static_cast<size_t>(T) * chunks;
   const int blocks = static_cast<int>((n + 255) / 256);
-  combine_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(y_perm), w, inv_perm, T, K, chunks,
-                                             reinterpret_cast<uint4*>(y));
+  const cudaError_t err = launch_kernel(combine_kernel, dim3(blocks), dim3(256), 0, stream, pdl,
+                                        reinterpret_cast<const uint4*>(y_perm), w, inv_perm, T, K, chunks,
+                                        reinterpret_cast<uint4*>(y));
   ++launch_counter();
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream) {

@@ -15,21 +15,32 @@ int& launch_counter();
 
 // ---- boundary (boundary.cu)
 // n >= 1 is the index of the residual add (coefficients sqrt((n-1)/n), 1/sqrt(n))
+// `pdl`: launch with programmatic stream serialization (every kernel waits for
+// its predecessor before reading its outputs or writing global memory).
 cudaError_t launch_boundary(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
-                            int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out, cudaStream_t stream);
+                            int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out, cudaStream_t stream,
+                            bool pdl = false, int* zero_slot = nullptr);
 bool boundary_supported(int H);
 
 // ---- router (router.cu)
 cudaError_t launch_router_logits(const uint16_t* z, const float* W, int T, int H, int E, float* logits,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, bool pdl = false);
+// Router and top-k in one launch (T <= 32, 256 experts in 8 groups): the last
+// block runs the selection. `ticket` must be zero on entry and is left zero.
+bool router_topk_fusable(int T, int E, int G);
+cudaError_t launch_router_topk_fused(const uint16_t* z, const float* W, const float* bias, int T, int H, int E,
+                                     int G, int TG, int K, float scale, float* logits, int32_t* ids, float* w,
+                                     int* ticket, cudaStream_t stream, bool pdl);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int G, int TG, int K, float scale,
-                        int32_t* ids, float* w, cudaStream_t stream);
+                        int32_t* ids, float* w, cudaStream_t stream, bool pdl = false);
 
 // ---- permutation (permute.cu)
 size_t permute_scratch_bytes(int T, int K, int E);
+// `clear` (optional): bytes zeroed before the permutation completes (the
+// experts' counters and tickets), inside the kernel at small sizes.
 cudaError_t launch_permute(const int32_t* ids, const uint16_t* z, int T, int K, int E, int H, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_perm, uint16_t* x_perm, void* scratch,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool pdl = false, void* clear = nullptr, size_t clear_bytes = 0);
 
 // ---- experts (experts.cu)
 struct GemmPlan {
@@ -44,11 +55,12 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms);
 // gate/up GEMM (one memset; each GEMM leaves its tickets at zero).
 size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down);
 cudaError_t clear_gemm_scratch(void* scratch, const GemmPlan& gate_up, const GemmPlan& down, cudaStream_t stream);
+size_t gemm_clear_bytes(const GemmPlan& gate_up, const GemmPlan& down);
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
-                        void* scratch, int num_sms, cudaStream_t stream);
+                        void* scratch, int num_sms, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,
-                           uint16_t* y, cudaStream_t stream);
+                           uint16_t* y, cudaStream_t stream, bool pdl = false);
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream);
 
 }  // namespace beam

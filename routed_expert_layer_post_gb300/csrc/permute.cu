@@ -20,6 +20,7 @@
 //            so the K copies of a token row hit L2.
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace beam {
 
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int hist[kMaxE];
   __shared__ int s_last;
   __shared__ int s_tot[kMaxE];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
   for (int e = tid; e < E; e += kThreads) hist[e] = 0;
@@ -93,6 +96,8 @@ __global__ void __launch_bounds__(kThreads)
     permute_scatter_kernel(const int32_t* __restrict__ ids, int total, int K, int E, const int* block_base,
                            int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_perm) {
   __shared__ int wcnt[kWarps][kMaxE];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int b = blockIdx.x;
   for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&wcnt[0][0])[i] = 0;
@@ -143,6 +148,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     gather_rows_kernel(const uint4* __restrict__ z, const int32_t* __restrict__ inv_perm, int total, int K,
                        int row_chunks, uint4* __restrict__ x_perm) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (i >= total) return;
@@ -151,6 +158,103 @@ __global__ void __launch_bounds__(kThreads)
   const size_t src = static_cast<size_t>(i / K) * row_chunks;
   const size_t dst = static_cast<size_t>(p) * row_chunks;
   for (int c = lane; c < row_chunks; c += 32) x_perm[dst + c] = z[src + c];
+}
+
+// Small batches (T*K <= kChunk): one kernel. Every block recomputes the
+// histogram, the scan and the stable positions of all pairs from the ids
+// (at most 2048 of them, cheap), block 0 writes offsets / perm_token /
+// inv_perm, and each block copies its share of rows into x_perm. No scratch,
+// no ticket, no memset: it replaces the three-kernel path at decode sizes.
+__global__ void __launch_bounds__(kThreads)
+    permute_small_kernel(const int32_t* __restrict__ ids, int total, int K, int E, const uint4* __restrict__ z,
+                         int row_chunks, int rows_per_block, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_perm, uint4* __restrict__ x_perm,
+                         int* __restrict__ clear, int clear_ints) {
+  __shared__ int s_ids[kChunk];
+  __shared__ int s_pos[kChunk];
+  __shared__ int wcnt[kWarps][kMaxE];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (blockIdx.x == 0)  // zero what the next kernels expect zeroed (the experts' counters and tickets)
+    for (int i = tid; i < clear_ints; i += kThreads) clear[i] = 0;
+  const int padded = ((total + kWarps * 32 - 1) / (kWarps * 32)) * kWarps * 32;
+  for (int i = tid; i < padded; i += kThreads) {
+    int e = i < total ? ids[i] : -1;
+    if (e >= E) e = -1;
+    s_ids[i] = e < 0 ? -1 : e;
+  }
+  for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&wcnt[0][0])[i] = 0;
+  __syncthreads();
+  // the pairs are split evenly over the warps (in order), 32 at a time
+  const int per_warp = ((total + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int wbeg = w * per_warp;
+  for (int j = 0; j < per_warp; j += 32) {  // per-warp counts
+    const int e = s_ids[wbeg + j + lane];
+    const unsigned peers = __match_any_sync(kFullMask, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[w][e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  if (w == 0) {  // exclusive scan over experts of the per-expert totals (warp 0, E <= 256)
+    const int per_lane = (E + 31) / 32;
+    int local = 0;
+    for (int j = 0; j < per_lane; ++j) {
+      const int e = lane * per_lane + j;
+      if (e < E) {
+        int t = 0;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) t += wcnt[ww][e];
+        local += t;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per_lane; ++j) {
+      const int e = lane * per_lane + j;
+      if (e < E) {
+        if (blockIdx.x == 0) offsets[e] = run;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) {  // counts -> exclusive prefix over warps
+          const int v = wcnt[ww][e];
+          wcnt[ww][e] = run;
+          run += v;
+        }
+      }
+    }
+    if (blockIdx.x == 0 && lane == 31) offsets[E] = incl;
+  }
+  __syncthreads();
+  for (int j = 0; j < per_warp; j += 32) {  // stable positions
+    const int i = wbeg + j + lane;
+    const int e = s_ids[i];
+    const unsigned peers = __match_any_sync(kFullMask, e);
+    int pos = -1;
+    if (e >= 0) pos = wcnt[w][e] + __popc(peers & lanemask_lt());
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[w][e] += __popc(peers);
+    __syncwarp();
+    s_pos[i] = pos;
+    if (blockIdx.x == 0 && i < total) {
+      inv_perm[i] = pos;
+      if (pos >= 0) perm_token[pos] = i / K;
+    }
+  }
+  __syncthreads();
+  if (x_perm == nullptr) return;
+  const int beg = blockIdx.x * rows_per_block, end = min(total, beg + rows_per_block);
+  for (int i = beg + w; i < end; i += kWarps) {  // one warp per row
+    const int pos = s_pos[i];
+    if (pos < 0) continue;
+    const size_t src = static_cast<size_t>(i / K) * row_chunks;
+    const size_t dst = static_cast<size_t>(pos) * row_chunks;
+    for (int c = lane; c < row_chunks; c += 32) x_perm[dst + c] = z[src + c];
+  }
 }
 
 }  // namespace
@@ -163,8 +267,22 @@ size_t permute_scratch_bytes(int T, int K, int E) {
 
 cudaError_t launch_permute(const int32_t* ids, const uint16_t* z, int T, int K, int E, int H, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_perm, uint16_t* x_perm, void* scratch,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool pdl, void* clear, size_t clear_bytes) {
   const int total = T * K;
+  if (total <= kChunk) {
+    const int rows_per_block = 16;
+    const int blocks = x_perm != nullptr ? (total + rows_per_block - 1) / rows_per_block : 1;
+    const cudaError_t err = launch_kernel(
+        permute_small_kernel, dim3(blocks), dim3(kThreads), 0, stream, pdl, ids, total, K, E,
+        reinterpret_cast<const uint4*>(z), H / 8, rows_per_block, offsets, perm_token, inv_perm,
+        reinterpret_cast<uint4*>(x_perm), static_cast<int*>(clear), static_cast<int>(clear_bytes / sizeof(int)));
+    ++launch_counter();
+    return err;
+  }
+  if (clear != nullptr && clear_bytes > 0) {
+    const cudaError_t err = cudaMemsetAsync(clear, 0, clear_bytes, stream);
+    if (err != cudaSuccess) return err;
+  }
   const int nb = (total + kChunk - 1) / kChunk;
   int* base = static_cast<int*>(scratch);
   int* ticket = base;                       // 64 ints reserved at the front

@@ -13,6 +13,7 @@
 // Arithmetic is plain fp32 FMA everywhere (no TF32, no bf16).
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace beam {
 
@@ -23,60 +24,8 @@ namespace {
 // row in registers and walks the tokens in groups of kTT.
 constexpr int kSmallThreads = 256;
 constexpr int kTT = 8;
-constexpr int kSmallMaxT = 32;
-
-constexpr int kMaxQ = 8192 / 4 / kSmallThreads;  // float4 slices of a row per thread (H <= 8192)
-
-__global__ void __launch_bounds__(kSmallThreads)
-    router_small_kernel(const uint16_t* __restrict__ z, const float* __restrict__ W, int T, int H, int E,
-                        float* __restrict__ logits) {
-  const int e = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int nq = H / 4;  // float4 chunks per row
-  const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
-  __shared__ float red[kSmallThreads / 32][kTT];
-
-  // the expert's weight row, read once for all tokens; every load is issued before any use
-  float4 w[kMaxQ];
-#pragma unroll
-  for (int i = 0; i < kMaxQ; ++i) {
-    const int q = tid + i * kSmallThreads;
-    w[i] = q < nq ? __ldg(wrow + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int t0 = 0; t0 < T; t0 += kTT) {
-    uint2 zz[kTT][kMaxQ];
-#pragma unroll
-    for (int t = 0; t < kTT; ++t)
-#pragma unroll
-      for (int i = 0; i < kMaxQ; ++i) {
-        const int q = tid + i * kSmallThreads;
-        zz[t][i] = (t0 + t < T && q < nq)
-                       ? *reinterpret_cast<const uint2*>(z + static_cast<size_t>(t0 + t) * H + 4 * q)
-                       : make_uint2(0u, 0u);
-      }
-#pragma unroll
-    for (int t = 0; t < kTT; ++t) {
-      float a = 0.f;
-#pragma unroll
-      for (int i = 0; i < kMaxQ; ++i) {
-        a = fmaf(bf16_lo(zz[t][i].x), w[i].x, a);
-        a = fmaf(bf16_hi(zz[t][i].x), w[i].y, a);
-        a = fmaf(bf16_lo(zz[t][i].y), w[i].z, a);
-        a = fmaf(bf16_hi(zz[t][i].y), w[i].w, a);
-      }
-      const float sum = warp_sum(a);
-      if ((tid & 31) == 0) red[tid >> 5][t] = sum;
-    }
-    __syncthreads();
-    if (tid < kTT && t0 + tid < T) {
-      float sum = 0.f;
-#pragma unroll
-      for (int w8 = 0; w8 < kSmallThreads / 32; ++w8) sum += red[w8][tid];
-      logits[static_cast<size_t>(t0 + tid) * E + e] = sum;
-    }
-    __syncthreads();
-  }
-}
+constexpr int kSmallMaxT = 128;  // one block per expert up to here
+constexpr int kFusedMaxT = 32;   // router + top-k in one launch up to here
 
 // ------------------------------------------------------------------ large T
 // Classic shared-memory SGEMM: block tile 64 tokens x 64 experts, k-slab 16,
@@ -88,6 +37,8 @@ __global__ void __launch_bounds__(256)
                         float* __restrict__ logits) {
   __shared__ __align__(16) float As[2][kBK][kBM + 4];
   __shared__ __align__(16) float Bs[2][kBK][kBN + 4];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int tid = threadIdx.x;
   const int m0 = blockIdx.x * kBM;
   const int n0 = blockIdx.y * kBN;
@@ -165,6 +116,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   __shared__ float s_gs[kTopkWarps][32];
   __shared__ float s_cs[kTopkWarps][kMaxK];
   __shared__ int s_ci[kTopkWarps][kMaxK];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int wi = threadIdx.x >> 5;
   const int t = blockIdx.x * kTopkWarps + wi;
@@ -232,26 +185,226 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   }
 }
 
+// Register top-k, for layouts where every group covers whole lanes: E = 32 *
+// EPL experts with lane l holding experts l*EPL .. l*EPL + EPL - 1, and a
+// group of E/G experts covering LPG = E/(G*EPL) consecutive lanes (Beam: EPL 8,
+// LPG 4). Group top-2 sums come from lane-local top-2 pairs merged across the
+// group's lanes; the TG groups are chosen by rank; the K experts by K rounds
+// of a warp argmax (ties to the lower index), which also yields the slot
+// order. The weights sum in slot order exactly as the generic kernel does.
+template <int EPL, int LPG>
+__device__ __forceinline__ void topk_lanes_token(const float* logits, const float* __restrict__ bias, int t, int G,
+                                                 int TG, int K, float scale, int32_t* __restrict__ ids,
+                                                 float* __restrict__ wout) {
+  const int lane = threadIdx.x & 31;
+  constexpr int E = 32 * EPL;
+  float s[EPL], sb[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane * EPL + i;
+    // L2 loads: the logits may have been written by other blocks of the same kernel
+    s[i] = 1.0f / (1.0f + expf(-__ldcg(logits + static_cast<size_t>(t) * E + e)));
+    sb[i] = s[i] + bias[e];
+  }
+  // group score: sum of the two largest biased scores of the group
+  float top1 = -INFINITY, top2 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    if (sb[i] > top1) {
+      top2 = top1;
+      top1 = sb[i];
+    } else if (sb[i] > top2) {
+      top2 = sb[i];
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < LPG; o <<= 1) {
+    const float b1 = __shfl_xor_sync(kFullMask, top1, o);
+    const float b2 = __shfl_xor_sync(kFullMask, top2, o);
+    const float n1 = fmaxf(top1, b1);
+    top2 = fmaxf(fminf(top1, b1), fmaxf(top2, b2));
+    top1 = n1;
+  }
+  const float gs = (EPL * LPG >= 2) ? top1 + top2 : top1;
+  const int my_group = lane / LPG;
+  int rank = 0;
+  for (int g = 0; g < G; ++g) {
+    const float o = __shfl_sync(kFullMask, gs, g * LPG);
+    rank += (o > gs) || (o == gs && g < my_group);
+  }
+  const bool chosen = rank < TG;  // same for every lane of a group
+  // K rounds of argmax over the chosen groups' experts
+  unsigned taken = 0;
+  float s_sel = 0.f;
+  int id_sel = 0;
+  float total = 0.f;
+  for (int k = 0; k < K; ++k) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    if (chosen) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        if (!((taken >> i) & 1u) && sb[i] > best) {  // strict: keeps the lower index on ties
+          best = sb[i];
+          bi = lane * EPL + i;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(kFullMask, best, o);
+      const int oi = __shfl_xor_sync(kFullMask, bi, o);
+      if (ov > best || (ov == best && oi < bi)) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    const int owner = bi / EPL;
+    float sv = 0.f;
+    if (lane == owner) {
+      const int i = bi - owner * EPL;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (j == i) sv = s[j];
+      taken |= 1u << i;
+    }
+    sv = __shfl_sync(kFullMask, sv, owner);
+    total += sv;
+    if (lane == k) {
+      s_sel = sv;
+      id_sel = bi;
+    }
+  }
+  if (lane < K) {
+    ids[static_cast<size_t>(t) * K + lane] = id_sel;
+    wout[static_cast<size_t>(t) * K + lane] = scale * s_sel / total;
+  }
+}
+
+template <int EPL, int LPG>
+__global__ void __launch_bounds__(kTopkWarps * 32)
+    topk_lanes_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int G, int TG,
+                      int K, float scale, int32_t* __restrict__ ids, float* __restrict__ wout) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_lanes_token<EPL, LPG>(logits, bias, t, G, TG, K, scale, ids, wout);
+}
+
+constexpr int kMaxQ = 8192 / 4 / kSmallThreads;  // float4 slices of a row per thread (H <= 8192)
+
+// With `ticket` set (Beam's 256 experts in 8 groups only), the last block to
+// finish also runs the register top-k for every token: the logits of all
+// experts are in L2 by then, and one launch is saved. The ticket must be zero
+// on entry (the layer's boundary kernel clears it); the last block leaves it
+// at zero.
+__global__ void __launch_bounds__(kSmallThreads)
+    router_small_kernel(const uint16_t* __restrict__ z, const float* __restrict__ W, int T, int H, int E,
+                        float* __restrict__ logits, const float* __restrict__ bias, int G, int TG, int K,
+                        float scale, int32_t* __restrict__ ids, float* __restrict__ wout, int* ticket) {
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nq = H / 4;  // float4 chunks per row
+  const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * H);
+  __shared__ float red[kSmallThreads / 32][kTT];
+
+  // the expert's weight row, read once for all tokens; every load is issued before any use
+  float4 w[kMaxQ];
+#pragma unroll
+  for (int i = 0; i < kMaxQ; ++i) {
+    const int q = tid + i * kSmallThreads;
+    w[i] = q < nq ? __ldg(wrow + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // the weights do not depend on the previous kernel; z does
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  for (int t0 = 0; t0 < T; t0 += kTT) {
+    uint2 zz[kTT][kMaxQ];
+#pragma unroll
+    for (int t = 0; t < kTT; ++t)
+#pragma unroll
+      for (int i = 0; i < kMaxQ; ++i) {
+        const int q = tid + i * kSmallThreads;
+        zz[t][i] = (t0 + t < T && q < nq)
+                       ? *reinterpret_cast<const uint2*>(z + static_cast<size_t>(t0 + t) * H + 4 * q)
+                       : make_uint2(0u, 0u);
+      }
+#pragma unroll
+    for (int t = 0; t < kTT; ++t) {
+      float a = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxQ; ++i) {
+        a = fmaf(bf16_lo(zz[t][i].x), w[i].x, a);
+        a = fmaf(bf16_hi(zz[t][i].x), w[i].y, a);
+        a = fmaf(bf16_lo(zz[t][i].y), w[i].z, a);
+        a = fmaf(bf16_hi(zz[t][i].y), w[i].w, a);
+      }
+      const float sum = warp_sum(a);
+      if ((tid & 31) == 0) red[tid >> 5][t] = sum;
+    }
+    __syncthreads();
+    if (tid < kTT && t0 + tid < T) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w8 = 0; w8 < kSmallThreads / 32; ++w8) sum += red[w8][tid];
+      logits[static_cast<size_t>(t0 + tid) * E + e] = sum;
+    }
+    __syncthreads();
+  }
+  if (ticket == nullptr) return;
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int t = tid >> 5; t < T; t += kSmallThreads / 32) topk_lanes_token<8, 4>(logits, bias, t, G, TG, K, scale, ids, wout);
+  if (tid == 0) *ticket = 0;
+}
+
 }  // namespace
 
 cudaError_t launch_router_logits(const uint16_t* z, const float* W, int T, int H, int E, float* logits,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool pdl) {
+  cudaError_t err;
   if (T <= kSmallMaxT) {
-    router_small_kernel<<<E, kSmallThreads, 0, stream>>>(z, W, T, H, E, logits);
+    err = launch_kernel(router_small_kernel, dim3(E), dim3(kSmallThreads), 0, stream, pdl, z, W, T, H, E, logits,
+                        static_cast<const float*>(nullptr), 0, 0, 0, 0.0f, static_cast<int32_t*>(nullptr),
+                        static_cast<float*>(nullptr), static_cast<int*>(nullptr));
   } else {
     dim3 grid((T + kBM - 1) / kBM, (E + kBN - 1) / kBN);
-    router_sgemm_kernel<<<grid, 256, 0, stream>>>(z, W, T, H, E, logits);
+    err = launch_kernel(router_sgemm_kernel, grid, dim3(256), 0, stream, pdl, z, W, T, H, E, logits);
   }
   ++launch_counter();
-  return cudaGetLastError();
+  return err;
+}
+
+bool router_topk_fusable(int T, int E, int G) { return T <= kFusedMaxT && E == 256 && G == 8; }
+
+cudaError_t launch_router_topk_fused(const uint16_t* z, const float* W, const float* bias, int T, int H, int E,
+                                     int G, int TG, int K, float scale, float* logits, int32_t* ids, float* w,
+                                     int* ticket, cudaStream_t stream, bool pdl) {
+  const cudaError_t err = launch_kernel(router_small_kernel, dim3(E), dim3(kSmallThreads), 0, stream, pdl, z, W, T,
+                                        H, E, logits, bias, G, TG, K, scale, ids, w, ticket);
+  ++launch_counter();
+  return err;
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int G, int TG, int K, float scale,
-                        int32_t* ids, float* w, cudaStream_t stream) {
+                        int32_t* ids, float* w, cudaStream_t stream, bool pdl) {
   const int blocks = (T + kTopkWarps - 1) / kTopkWarps;
-  topk_kernel<<<blocks, kTopkWarps * 32, 0, stream>>>(logits, bias, T, E, G, TG, K, scale, ids, w);
+  cudaError_t err;
+  if (E == 256 && G == 8) {  // Beam's layout: 8 experts per lane, a group is 4 lanes
+    err = launch_kernel(topk_lanes_kernel<8, 4>, dim3(blocks), dim3(kTopkWarps * 32), 0, stream, pdl, logits, bias,
+                        T, G, TG, K, scale, ids, w);
+  } else {
+    err = launch_kernel(topk_kernel, dim3(blocks), dim3(kTopkWarps * 32), 0, stream, pdl, logits, bias, T, E, G, TG,
+                        K, scale, ids, w);
+  }
   ++launch_counter();
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace beam
