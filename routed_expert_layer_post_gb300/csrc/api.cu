@@ -147,13 +147,21 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
   cudaError_t e = cudaSuccess;
   if (!cleared && (e = beam::clear_gemm_scratch(g, p0, p1, s)) != cudaSuccess) return BEAM_ERR_CUDA;
   record(dbg, 3, s);
-  e = beam::launch_gemm(0, p0, p1, w_gu, x_perm, offsets, rows, c->num_experts, c->hidden, c->d_ff, act, g, sms, s,
-                        pdl);
-  if (e != cudaSuccess) return BEAM_ERR_CUDA;
-  record(dbg, 4, s);
-  e = beam::launch_gemm(1, p0, p1, w_d, act, offsets, rows, c->num_experts, c->hidden, c->d_ff, y_perm, g, sms, s,
-                        pdl);
-  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  if (beam::fused_experts_supported(p0, p1)) {
+    // both GEMMs in one launch (the per-stage events bracket it as gate/up; down reads 0)
+    e = beam::launch_fused_experts(p0, p1, w_gu, w_d, x_perm, offsets, rows, c->num_experts, c->hidden, c->d_ff,
+                                   act, y_perm, g, sms, s, pdl);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    record(dbg, 4, s);
+  } else {
+    e = beam::launch_gemm(0, p0, p1, w_gu, x_perm, offsets, rows, c->num_experts, c->hidden, c->d_ff, act, g, sms,
+                          s, pdl);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    record(dbg, 4, s);
+    e = beam::launch_gemm(1, p0, p1, w_d, act, offsets, rows, c->num_experts, c->hidden, c->d_ff, y_perm, g, sms, s,
+                          pdl);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
   record(dbg, 5, s);
   e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, pdl);
   record(dbg, 6, s);

@@ -90,15 +90,6 @@ __device__ __forceinline__ F2 rsqrt_mean(F2 sum, double inv_h, double eps) {
   return {hi, static_cast<float>(r - static_cast<double>(hi))};
 }
 
-// warp-wide: every lane holds the same sum; lane 0 evaluates, all lanes receive
-__device__ __forceinline__ F2 warp_rsqrt_mean(F2 sum, double inv_h, double eps) {
-  F2 r{0.f, 0.f};
-  if ((threadIdx.x & 31) == 0) r = rsqrt_mean(sum, inv_h, eps);
-  r.hi = __shfl_sync(kFullMask, r.hi, 0);
-  r.lo = __shfl_sync(kFullMask, r.lo, 0);
-  return r;
-}
-
 // bf16 bits of the exact value hi + lo, where |lo| <= half an fp32 ulp of hi
 __device__ __forceinline__ uint32_t round_pair(float hi, float lo) {
   const uint32_t b = __float_as_uint(hi);
@@ -110,9 +101,7 @@ __device__ __forceinline__ uint32_t round_pair(float hi, float lo) {
 }
 
 // bf16 bits of a * b * r with a, b bf16 values (a * b exact in fp32) and r a pair
-// (out of line: it is the rarely taken exact path, and inlining it into every
-// element bloats the kernel past the instruction cache)
-__device__ __noinline__ uint32_t scaled_bf16(float a, float b, const F2& r) {
+__device__ __forceinline__ uint32_t scaled_bf16(float a, float b, const F2& r) {
   const float ab = __fmul_rn(a, b);
   const float p = __fmul_rn(ab, r.hi);
   float pe = fmaf(ab, r.hi, -p);
@@ -127,8 +116,8 @@ struct ResidualCoef {
   float cm_hi, cm_lo, c_hi, c_lo;
 };
 
-// bf16 bits of (sqrt(n-1) h + y) / sqrt(n) (out of line, as above)
-__device__ __noinline__ uint32_t residual_bf16(float h, float y, const ResidualCoef& k) {
+// bf16 bits of (sqrt(n-1) h + y) / sqrt(n)
+__device__ __forceinline__ uint32_t residual_bf16(float h, float y, const ResidualCoef& k) {
   const float p = __fmul_rn(k.cm_hi, h);
   float pe = fmaf(k.cm_hi, h, -p);
   pe = fmaf(k.cm_lo, h, pe);

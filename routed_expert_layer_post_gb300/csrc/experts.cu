@@ -56,22 +56,33 @@ constexpr uint64_t kDrainNs = 50000000ull;      // 50 ms while unwinding
 constexpr int kQueue = 8;                       // depth of the work-unit queue in shared memory
 constexpr int kMaxSplit = 20;                   // largest split-K factor (partials summed from registers)
 
-struct GemmParams {
+// One GEMM phase: gate/up (kind 0: two accumulators, SwiGLU epilogue) or
+// down (kind 1: one accumulator).
+struct PhaseParams {
   CUtensorMap tmap_w;   // weights, 3-D: (k, row, expert)
   CUtensorMap tmap_x;   // activations, 2-D: (k, permuted row)
-  const int32_t* offsets;
   uint16_t* out;
-  float* partials;
-  int* tickets;
-  int* counter;   // dynamic unit counter (zero before the launch)
+  float* partials;      // split-K partial sums of this phase
+  int* tickets;         // split-K tickets of this phase (zero before the launch)
+  int n_mb;             // 128-row weight blocks per expert
+  int ksteps;           // reduction length / 64
+  int split;            // split-K factor
+  int out_ld;           // output row length (F for gate/up, H for down)
+  int up_row;           // first up row inside [2F] (gate/up)
+  int max_tiles;        // tiles the workspace was sized for
+};
+
+// MODE 0: gate/up only; MODE 1: down only; MODE 2: both phases in one launch
+// (phase 0 = gate/up, phase 1 = down), the down units of a token tile waiting
+// for the gate/up tiles that produce its rows.
+struct GemmParams {
+  PhaseParams ph[2];
+  const int32_t* offsets;
+  int* counter;          // dynamic unit counter (zero before the launch)
+  int* done;             // MODE 2: gate/up row blocks finished per token tile (zero before the launch)
   int E;
-  int rows;       // permuted rows (T * K)
-  int n_mb;       // 128-row weight blocks per expert
-  int ksteps;     // reduction length / 64
-  int split;      // split-K factor
-  int out_ld;     // output row length (F for mode 0, H for mode 1)
-  int up_row;     // first up row inside [2F] (mode 0)
-  int max_tiles;  // tiles the workspace was sized for
+  int rows;              // permuted rows (T * K)
+  int max_token_tiles;   // MODE 2: size of `done`
 };
 
 constexpr int pow2_at_least(int v) {
@@ -82,13 +93,19 @@ constexpr int pow2_at_least(int v) {
 
 template <int MODE, int BN>
 struct Cfg {
-  static constexpr int kNAcc = MODE == 0 ? 2 : 1;
+  static constexpr int kNAcc = MODE == 1 ? 1 : 2;   // accumulators of the widest phase
   static constexpr int kTileBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kNAcc * kTileABytes + kTileBBytes;
+  // MODE 2 keeps a second activation slot so that a down unit can fill a
+  // stage with two k-steps (two weight tiles, two activation tiles)
+  static constexpr int kBSlots = MODE == 2 ? 2 : 1;
+  static constexpr int kStageBytes = kNAcc * kTileABytes + kBSlots * kTileBBytes;
   static constexpr int kStagesRaw = (kSmemLimit - 1024 - kCtrlBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kAccCols = kNAcc * BN;
-  static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
+  // two accumulator buffers in TMEM: the epilogue of one tile overlaps the
+  // MMAs of the next (four were measured slower at decode)
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
@@ -115,38 +132,82 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-__device__ __forceinline__ void decode_unit(int u, int split, int E, const int* s_tstart, const int* s_ntt, int& e,
-                                            int& mb, int& tt, int& s, int& tile) {
-  tile = u / split;
-  s = u - tile * split;
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_tstart[mid] <= tile) lo = mid; else hi = mid - 1;
-  }
-  e = lo;
-  const int local = tile - s_tstart[e];
-  const int ntt = s_ntt[e];
-  mb = local / ntt;
-  tt = local - mb * ntt;
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-template <int MODE, int BN>
-__device__ __forceinline__ void store_outputs(const GemmParams& p, const float (&v)[2][16], int c0, int valid,
-                                              int row0, int col) {
+// Wait (bounded) until *counter >= target; other CTAs of this launch raise it.
+__device__ __forceinline__ bool wait_counter(const int* counter, int target, volatile int* abort_flag, int site) {
+  if (ld_acquire(counter) >= target) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire(counter) >= target) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicCAS(&g_device_error, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+// A work unit: phase, expert e, weight row block mb, token tile tt (and its
+// global index gtt), split s, and the phase-local tile index.
+struct Unit {
+  int phase, e, mb, tt, gtt, s, tile;
+};
+
+// Tiles of a phase are laid out expert by expert, row block by row block,
+// token tile fastest; expert e's tiles start at n_mb * s_ttstart[e].
+__device__ __forceinline__ Unit decode_unit(int u, int n_units0, const GemmParams& p, const int* s_ttstart,
+                                            const int* s_ntt) {
+  Unit r;
+  r.phase = (u < n_units0) ? 0 : 1;
+  const PhaseParams& ph = p.ph[r.phase];
+  const int v = r.phase == 0 ? u : u - n_units0;
+  r.tile = v / ph.split;
+  r.s = v - r.tile * ph.split;
+  const int q = r.tile / ph.n_mb;
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_ttstart[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  r.e = lo;
+  const int local = r.tile - ph.n_mb * s_ttstart[r.e];
+  const int ntt = s_ntt[r.e];
+  r.mb = local / ntt;
+  r.tt = local - r.mb * ntt;
+  r.gtt = s_ttstart[r.e] + r.tt;
+  return r;
+}
+
+template <int MODE>
+__device__ __forceinline__ int unit_kind(int phase) {
+  return MODE == 2 ? phase : MODE;
+}
+
+template <int BN>
+__device__ __forceinline__ void store_outputs(const PhaseParams& ph, int rows, int kind, const float (&v)[2][16],
+                                              int c0, int valid, int row0, int col) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (c0 + j < valid) {
       const int row = row0 + c0 + j;
-      if (row >= 0 && row < p.rows) {
+      if (row >= 0 && row < rows) {
         float val;
-        if (MODE == 0) {
+        if (kind == 0) {
           const float g = v[0][j];
           val = g / (1.0f + __expf(-g)) * v[1][j];
         } else {
           val = v[0][j];
         }
-        p.out[static_cast<size_t>(row) * p.out_ld + col] = static_cast<uint16_t>(f2bf(val));
+        ph.out[static_cast<size_t>(row) * ph.out_ld + col] = static_cast<uint16_t>(f2bf(val));
       }
     }
   }
@@ -162,17 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + C::kStages;
   uint64_t* tfull = empty + C::kStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* qfull = tempty + 2;
+  uint64_t* tempty = tfull + 4;
+  uint64_t* qfull = tempty + 4;
   uint64_t* qempty = qfull + kQueue;
   uint64_t* drain = qempty + kQueue;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  // [0] abort, [1] last arriver, [2] tile ready, [3] current unit (epilogue broadcast)
+  // [0] abort, [1] last arriver, [3] current unit (epilogue broadcast)
   int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
   int* s_queue = s_flags + 4;
   int* s_off = s_queue + kQueue;
   int* s_ntt = s_off + kMaxE + 1;
-  int* s_tstart = s_ntt + kMaxE;
+  int* s_ttstart = s_ntt + kMaxE;
   volatile int* abort_flag = s_flags;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       ptx::mbar_init(&full[i], 1);
       ptx::mbar_init(&empty[i], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::kAccBufs; ++a) {
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], 128);
     }
@@ -194,27 +255,31 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(&p.tmap_w);
-    ptx::prefetch_tensormap(&p.tmap_x);
+    ptx::prefetch_tensormap(&p.ph[0].tmap_w);
+    ptx::prefetch_tensormap(&p.ph[0].tmap_x);
+    if (MODE == 2) {
+      ptx::prefetch_tensormap(&p.ph[1].tmap_w);
+      ptx::prefetch_tensormap(&p.ph[1].tmap_x);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, C::kTmemCols);
     ptx::tmem_relinquish();
   }
   // Programmatic dependent launch: everything above overlaps the previous
-  // kernel. The gate/up GEMM reads that kernel's outputs (offsets, x_perm)
-  // and waits here. The down GEMM's offsets and weights come from earlier
-  // kernels (its predecessor only waits for them), so it builds its tile
-  // table and streams weight tiles now; only its activation loads and its
-  // epilogue wait for the gate/up GEMM.
-  if (MODE == 0) {
+  // kernel. MODES 0 and 2 read that kernel's outputs (offsets, x_perm) and
+  // wait here. The separate down GEMM (MODE 1) reads offsets and weights
+  // written before its predecessor started, so it builds its tile table and
+  // streams weight tiles now; only its activation loads and its epilogue wait
+  // for the gate/up GEMM.
+  if (MODE != 1) {
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
   }
   for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
   __syncthreads();
   if (warp == 0) {
-    // tiles per expert and their exclusive prefix (lane l owns a contiguous block of experts)
+    // token tiles per expert and their exclusive prefix (lane l owns a contiguous block of experts)
     const int per_lane = (p.E + 31) / 32;
     int local = 0;
     for (int j = 0; j < per_lane; ++j) {
@@ -223,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const int cnt = max(0, s_off[e + 1] - s_off[e]);
         const int ntt = (cnt + BN - 1) / BN;
         s_ntt[e] = ntt;
-        local += ntt * p.n_mb;
+        local += ntt;
       }
     }
     int incl = local;
@@ -236,27 +301,34 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     for (int j = 0; j < per_lane; ++j) {
       const int e = lane * per_lane + j;
       if (e < p.E) {
-        s_tstart[e] = run;
-        run += s_ntt[e] * p.n_mb;
+        s_ttstart[e] = run;
+        run += s_ntt[e];
       }
     }
-    if (lane == 31) s_tstart[p.E] = incl;
+    if (lane == 31) s_ttstart[p.E] = incl;
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  int n_tiles = s_tstart[p.E];
-  if (n_tiles > p.max_tiles) {
+  const int n_tt = s_ttstart[p.E];
+  int n_tiles0 = n_tt * p.ph[0].n_mb;
+  if (n_tiles0 > p.ph[0].max_tiles || (MODE == 2 && n_tt > p.max_token_tiles)) {
     if (tid == 0) atomicCAS(&g_device_error, 0, 100);
-    n_tiles = p.max_tiles;
+    n_tiles0 = 0;  // workspace too small for this routing: do nothing rather than overrun it
   }
-  const int n_units = n_tiles * p.split;
+  const int n_units0 = n_tiles0 * p.ph[0].split;
+  int n_units = n_units0;
+  if (MODE == 2 && n_tiles0 > 0) {
+    const int n_tiles1 = n_tt * p.ph[1].n_mb;
+    if (n_tiles1 <= p.ph[1].max_tiles) n_units += n_tiles1 * p.ph[1].split;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler + TMA producer
     // Units are handed out dynamically: the first one is blockIdx.x, the
-    // rest come from a global counter, so SMs that stream faster take more
+    // rest come from a global counter (the next id is requested while the
+    // current unit's loads are issued), so SMs that stream faster take more
     // units and all SMs finish together. Each unit id is published to the
     // MMA and epilogue warps through a small queue in shared memory.
     if (lane == 0) {
@@ -266,20 +338,21 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      // mode 1: activation (B) loads wait for the previous kernel; until then
+      // MODE 1: activation (B) loads wait for the previous kernel; until then
       // stages get their weight tile only and are remembered here
-      bool dep_ready = (MODE == 0);
+      bool dep_ready = (MODE != 1);
       int npend = 0;
       int pend_stage[C::kStages], pend_k[C::kStages], pend_row[C::kStages];
       auto release_pending = [&]() {
         ptx::griddep_wait();
         ptx::griddep_launch_dependents();
         for (int i = 0; i < npend; ++i)
-          ptx::tma_load_2d(tiles + pend_stage[i] * C::kStageBytes + C::kNAcc * kTileABytes, &p.tmap_x,
+          ptx::tma_load_2d(tiles + pend_stage[i] * C::kStageBytes + C::kNAcc * kTileABytes, &p.ph[0].tmap_x,
                            &full[pend_stage[i]], pend_k[i] * kBK, pend_row[i], pol_x);
         npend = 0;
         dep_ready = true;
       };
+      int ready_gtt = -1;  // MODE 2: the last token tile whose gate/up rows were seen complete
       int u_next = static_cast<int>(blockIdx.x);
       for (int seq = 0;; ++seq) {
         int u = u_next;
@@ -295,22 +368,55 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         if (u < 0) break;
         // ask for the following unit now: the atomic's round trip overlaps this unit's loads
         u_next = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
-        int e, mb, tt, s, tile;
-        decode_unit(u, p.split, p.E, s_tstart, s_ntt, e, mb, tt, s, tile);
-        const int k0 = s * p.ksteps / p.split, k1 = (s + 1) * p.ksteps / p.split;
-        const int row0 = s_off[e] + tt * BN;
-        for (int k = k0; k < k1; ++k) {
+        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
+        const PhaseParams& ph = p.ph[w.phase];
+        const int kind = unit_kind<MODE>(w.phase);
+        const int nacc = kind == 0 ? 2 : 1;
+        const uint32_t stage_bytes = nacc * kTileABytes + C::kTileBBytes;
+        const int k0 = w.s * ph.ksteps / ph.split, k1 = (w.s + 1) * ph.ksteps / ph.split;
+        const int row0 = s_off[w.e] + w.tt * BN;
+        if (MODE == 2 && w.phase == 1 && w.gtt != ready_gtt) {
+          // this token tile's rows of `act` come from gate/up units held by
+          // running CTAs (all gate/up units are handed out before any down unit)
+          if (!wait_counter(p.done + w.gtt, p.ph[0].n_mb, abort_flag, 8)) {
+            ok = false;
+            continue;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
+          ready_gtt = w.gtt;
+        }
+        // k-steps per stage: 1, or 2 for down units of the fused launch
+        const int kps = (MODE == 2 && kind == 1) ? 2 : 1;
+        for (int k = k0; k < k1; k += kps) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, 1, kTimeoutNs)) {
             ok = false;
             break;
           }
           uint8_t* st = tiles + stage * C::kStageBytes;
-          ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          ptx::tma_load_3d(st, &p.tmap_w, &full[stage], k * kBK, mb * kBM, e, pol_w);
-          if (MODE == 0)
-            ptx::tma_load_3d(st + kTileABytes, &p.tmap_w, &full[stage], k * kBK, p.up_row + mb * kBM, e, pol_w);
+          if (kps == 2) {
+            const bool two = k + 1 < k1;
+            ptx::mbar_arrive_expect_tx(&full[stage], (two ? 2u : 1u) * (kTileABytes + C::kTileBBytes));
+            ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e, pol_w);
+            ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &ph.tmap_x, &full[stage], k * kBK, row0, pol_x);
+            if (two) {
+              ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], (k + 1) * kBK, w.mb * kBM, w.e, pol_w);
+              ptx::tma_load_2d(st + C::kNAcc * kTileABytes + C::kTileBBytes, &ph.tmap_x, &full[stage],
+                               (k + 1) * kBK, row0, pol_x);
+            }
+            ++issued;
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
+          ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e, pol_w);
+          if (kind == 0)
+            ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], k * kBK, ph.up_row + w.mb * kBM, w.e,
+                             pol_w);
           if (dep_ready) {
-            ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &p.tmap_x, &full[stage], k * kBK, row0, pol_x);
+            ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &ph.tmap_x, &full[stage], k * kBK, row0, pol_x);
           } else {
             pend_stage[npend] = stage;
             pend_k[npend] = k;
@@ -346,14 +452,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         if (wait_bar(&qfull[slot], (seq / kQueue) & 1, abort_flag, 6, kTimeoutNs)) u = s_queue[slot];
         ptx::mbar_arrive(&qempty[slot]);
         if (u < 0) break;
-        int e, mb, tt, s, tile;
-        decode_unit(u, p.split, p.E, s_tstart, s_ntt, e, mb, tt, s, tile);
-        const int k0 = s * p.ksteps / p.split, k1 = (s + 1) * p.ksteps / p.split;
+        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
+        const PhaseParams& ph = p.ph[w.phase];
+        const int kind = unit_kind<MODE>(w.phase);
+        const int nacc = kind == 0 ? 2 : 1;
+        const int k0 = w.s * ph.ksteps / ph.split, k1 = (w.s + 1) * ph.ksteps / ph.split;
+        const int kps = (MODE == 2 && kind == 1) ? 2 : 1;
         if (!wait_bar(&tempty[acc], acc_phase ^ 1u, abort_flag, 2, kTimeoutNs)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
         bool ok = true;
-        for (int k = k0; k < k1; ++k) {
+        for (int k = k0; k < k1; k += kps) {
           if (!wait_bar(&full[stage], phase, abort_flag, 3, kTimeoutNs)) {
             ok = false;
             break;
@@ -361,13 +470,28 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_u32(tiles + stage * C::kStageBytes);
           const uint32_t sb = sa + C::kNAcc * kTileABytes;
+          if (kps == 2) {
+            // two k-steps of one accumulator: (A0, B0) then (A1, B1)
+            const int nk = (k + 1 < k1) ? 2 : 1;
+            for (int h = 0; h < nk; ++h) {
 #pragma unroll
-          for (int j = 0; j < kBK / 16; ++j) {
-            const uint64_t bdesc = ptx::smem_desc_k128(sb + j * 32);
+              for (int j = 0; j < kBK / 16; ++j) {
+                const uint64_t bdesc = ptx::smem_desc_k128(sb + h * C::kTileBBytes + j * 32);
+                const uint64_t adesc = ptx::smem_desc_k128(sa + h * kTileABytes + j * 32);
+                ptx::mma_bf16(d, adesc, bdesc, idesc, (k > k0 || h > 0 || j > 0) ? 1u : 0u);
+              }
+            }
+          } else {
 #pragma unroll
-            for (int a = 0; a < C::kNAcc; ++a) {
-              const uint64_t adesc = ptx::smem_desc_k128(sa + a * kTileABytes + j * 32);
-              ptx::mma_bf16(d + a * BN, adesc, bdesc, idesc, (k > k0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < kBK / 16; ++j) {
+              const uint64_t bdesc = ptx::smem_desc_k128(sb + j * 32);
+#pragma unroll
+              for (int a = 0; a < C::kNAcc; ++a) {
+                if (a < nacc) {
+                  const uint64_t adesc = ptx::smem_desc_k128(sa + a * kTileABytes + j * 32);
+                  ptx::mma_bf16(d + a * BN, adesc, bdesc, idesc, (k > k0 || j > 0) ? 1u : 0u);
+                }
+              }
             }
           }
           ptx::mma_commit(&empty[stage]);
@@ -378,8 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         }
         if (!ok) break;
         ptx::mma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == C::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // every MMA issued by this thread has completed once `drain` flips
       ptx::mma_commit(drain);
@@ -409,38 +535,45 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       ptx::named_bar_sync(1, 128);
       if (u < 0) break;
       ptx::tc_fence_after();
-      int e, mb, tt, s, tile;
-      decode_unit(u, p.split, p.E, s_tstart, s_ntt, e, mb, tt, s, tile);
-      const int row0 = s_off[e] + tt * BN;
-      const int valid = min(BN, s_off[e + 1] - row0);
-      const int col = mb * kBM + m;
+      const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
+      const PhaseParams& ph = p.ph[w.phase];
+      const int kind = unit_kind<MODE>(w.phase);
+      const int nacc = kind == 0 ? 2 : 1;
+      const int row0 = s_off[w.e] + w.tt * BN;
+      const int valid = min(BN, s_off[w.e + 1] - row0);
+      const int col = w.mb * kBM + m;
       const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * C::kAccCols);
-      if (p.split == 1) {
+      bool tile_done = false;  // this unit completed its tile's outputs
+      if (ph.split == 1) {
         for (int c0 = 0; c0 < valid; c0 += 16) {
           uint32_t r[2][16];
 #pragma unroll
-          for (int a = 0; a < C::kNAcc; ++a) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
+          for (int a = 0; a < C::kNAcc; ++a)
+            if (a < nacc) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
           ptx::tmem_ld_wait();
           float v[2][16];
 #pragma unroll
           for (int a = 0; a < 2; ++a)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[a][j] = a < C::kNAcc ? __uint_as_float(r[a][j]) : 0.f;
-          store_outputs<MODE, BN>(p, v, c0, valid, row0, col);
+            for (int j = 0; j < 16; ++j) v[a][j] = (a < C::kNAcc && a < nacc) ? __uint_as_float(r[a][j]) : 0.f;
+          store_outputs<BN>(ph, p.rows, kind, v, c0, valid, row0, col);
         }
+        tile_done = true;
       } else {
-        const size_t slot_elems = static_cast<size_t>(C::kAccCols) * kBM;
-        float* mine = p.partials + (static_cast<size_t>(tile) * p.split + s) * slot_elems;
+        const size_t slot_elems = static_cast<size_t>(nacc * BN) * kBM;
+        float* mine = ph.partials + (static_cast<size_t>(w.tile) * ph.split + w.s) * slot_elems;
         for (int c0 = 0; c0 < valid; c0 += 16) {
           uint32_t r[2][16];
 #pragma unroll
-          for (int a = 0; a < C::kNAcc; ++a) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
+          for (int a = 0; a < C::kNAcc; ++a)
+            if (a < nacc) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int a = 0; a < C::kNAcc; ++a)
+            if (a < nacc)
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < valid) mine[static_cast<size_t>(a * BN + c0 + j) * kBM + m] = __uint_as_float(r[a][j]);
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < valid) mine[static_cast<size_t>(a * BN + c0 + j) * kBM + m] = __uint_as_float(r[a][j]);
         }
         // the barrier orders every thread's partial stores before the
         // leader's fence; the fence (cumulative) then publishes them before
@@ -449,18 +582,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         ptx::named_bar_sync(1, 128);
         if (leader) {
           __threadfence();
-          const int last_now = (atomicAdd(&p.tickets[tile], 1) == p.split - 1) ? 1 : 0;
+          const int last_now = (atomicAdd(&ph.tickets[w.tile], 1) == ph.split - 1) ? 1 : 0;
           if (last_now) __threadfence();
           s_flags[1] = last_now;
         }
         ptx::named_bar_sync(1, 128);
         const int last = *reinterpret_cast<volatile int*>(&s_flags[1]);
         if (last) {
-          const float* tile_parts = p.partials + static_cast<size_t>(tile) * p.split * slot_elems;
+          const float* tile_parts = ph.partials + static_cast<size_t>(w.tile) * ph.split * slot_elems;
           for (int c0 = 0; c0 < valid; c0 += 16) {
             uint32_t r[2][16];
 #pragma unroll
-            for (int a = 0; a < C::kNAcc; ++a) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
+            for (int a = 0; a < C::kNAcc; ++a)
+              if (a < nacc) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
             ptx::tmem_ld_wait();
             float v[2][16];
 #pragma unroll
@@ -476,10 +610,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
 #pragma unroll
                 for (int ss = 0; ss < kMaxSplit; ++ss)
-                  x[a][ss] = (ss < p.split && ss != s) ? __ldcg(tile_parts + ss * slot_elems + off) : 0.f;
+                  x[a][ss] = (a < nacc && ss < ph.split && ss != w.s)
+                                 ? __ldcg(tile_parts + ss * slot_elems + off) : 0.f;
               }
 #pragma unroll
               for (int a = 0; a < C::kNAcc; ++a) {
+                if (a >= nacc) continue;
                 float mine_v = 0.f;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
@@ -487,8 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 float sum = 0.f;
 #pragma unroll
                 for (int ss = 0; ss < kMaxSplit; ++ss) {
-                  if (ss < p.split) {
-                    const float xv = (ss == s) ? mine_v : x[a][ss];
+                  if (ss < ph.split) {
+                    const float xv = (ss == w.s) ? mine_v : x[a][ss];
                     sum = (ss == 0) ? xv : sum + xv;
                   }
                 }
@@ -497,16 +633,27 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                   if (jj == j) v[a][jj] = sum;
               }
             }
-            store_outputs<MODE, BN>(p, v, c0, valid, row0, col);
+            store_outputs<BN>(ph, p.rows, kind, v, c0, valid, row0, col);
           }
-          if (leader) p.tickets[tile] = 0;
+          if (leader) ph.tickets[w.tile] = 0;
+          tile_done = true;
         }
         ptx::named_bar_sync(1, 128);
       }
+      if (MODE == 2 && w.phase == 0 && tile_done) {
+        // publish this row block of the token tile to the down units waiting on it
+        ptx::named_bar_sync(1, 128);
+        if (leader) {
+          __threadfence();
+          atomicAdd(p.done + w.gtt, 1);
+        }
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == C::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 
@@ -615,6 +762,18 @@ cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t st
   }
 }
 
+// the down GEMM also has a 256-token tile (its single accumulator fits TMEM twice)
+template <>
+cudaError_t launch_mode<1>(int bn, const GemmParams& prm, int grid, cudaStream_t stream, bool pdl) {
+  switch (bn) {
+    case 16: return launch_mode_bn<1, 16>(prm, grid, stream, pdl);
+    case 32: return launch_mode_bn<1, 32>(prm, grid, stream, pdl);
+    case 64: return launch_mode_bn<1, 64>(prm, grid, stream, pdl);
+    case 128: return launch_mode_bn<1, 128>(prm, grid, stream, pdl);
+    default: return launch_mode_bn<1, 256>(prm, grid, stream, pdl);
+  }
+}
+
 int accum_cols(int mode, int bn) { return (mode == 0 ? 2 : 1) * bn; }
 
 }  // namespace
@@ -624,12 +783,17 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms) {
   const long long entries = static_cast<long long>(T) * K;
   const long long touched = entries < E ? entries : E;
   const double r = touched > 0 ? static_cast<double>(entries) / static_cast<double>(touched) : 1.0;
+  // token tile: the smallest width holding the mean rows per expert with some
+  // slack; up to 128 for gate/up (two accumulators) and 256 for down, where
+  // the wider tile halves the operand bytes per MMA at prefill sizes
+  const int bn_max = mode == 0 ? 128 : 256;
   int bn = 16;
-  while (bn < 128 && 1.25 * r > bn) bn <<= 1;
+  while (bn < bn_max && 1.25 * r > bn) bn <<= 1;
   const int n_mb = mode == 0 ? F / kBM : H / kBM;
   const int ksteps = mode == 0 ? H / kBK : F / kBK;
   plan.bn = bn;
-  plan.max_tiles = static_cast<int>((touched + entries / bn) * n_mb);
+  plan.max_token_tiles = static_cast<int>(touched + entries / bn);
+  plan.max_tiles = plan.max_token_tiles * n_mb;
   const long long per_expert = static_cast<long long>((r + bn - 1) / bn);
   const long long est = touched * (per_expert > 0 ? per_expert : 1) * n_mb;
   // Units are handed out dynamically, so balance depends on how small the
@@ -653,31 +817,80 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms) {
 
 namespace {
 
-// Scratch shared by the gate/up and down GEMMs of one experts pass:
-//   [0, 256)                     two dynamic unit counters (one per GEMM)
-//   [256, 256 + tickets)         split-K tickets, sized for the larger plan
-//   [.., ..)                     split-K partial sums, sized for the larger plan
+// Scratch shared by one gate/up + down pass:
+//   [0, 256)      the dynamic unit counters (one per launch)
+//   tickets0/1    split-K tickets of each phase
+//   done          gate/up row blocks finished per token tile (fused launch)
+//   partials0/1   split-K partial sums of each phase
+// Everything before partials0 must be zero when the pass starts.
 constexpr size_t kCounterBytes = 256;
 
-size_t ticket_bytes(const GemmPlan& g, const GemmPlan& d) {
-  const int cap = g.max_tiles > d.max_tiles ? g.max_tiles : d.max_tiles;
-  return (static_cast<size_t>(cap) * sizeof(int) + 255) & ~static_cast<size_t>(255);
-}
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 size_t partial_bytes(int mode, const GemmPlan& plan) {
   if (plan.split <= 1) return 0;
   return static_cast<size_t>(plan.max_tiles) * plan.split * accum_cols(mode, plan.bn) * kBM * sizeof(float);
 }
 
+struct ScratchLayout {
+  size_t tickets0, tickets1, done, partials0, partials1, total;
+};
+
+ScratchLayout scratch_layout(const GemmPlan& g, const GemmPlan& d) {
+  ScratchLayout l{};
+  const int max_tt = g.max_token_tiles > d.max_token_tiles ? g.max_token_tiles : d.max_token_tiles;
+  l.tickets0 = kCounterBytes;
+  l.tickets1 = l.tickets0 + align256(static_cast<size_t>(g.max_tiles) * sizeof(int));
+  l.done = l.tickets1 + align256(static_cast<size_t>(d.max_tiles) * sizeof(int));
+  l.partials0 = l.done + align256(static_cast<size_t>(max_tt) * sizeof(int));
+  l.partials1 = l.partials0 + align256(partial_bytes(0, g));
+  l.total = l.partials1 + align256(partial_bytes(1, d));
+  return l;
+}
+
+bool fill_phase(PhaseParams& ph, int mode, const GemmPlan& plan, const uint16_t* weights, const uint16_t* act_in,
+                int rows, int E, int H, int F, uint16_t* out, char* base, const ScratchLayout& l) {
+  const int kdim = mode == 0 ? H : F;  // reduction length
+  const int wrows = mode == 0 ? 2 * F : H;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(wrows),
+                                static_cast<cuuint64_t>(E)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kdim) * 2,
+                                   static_cast<cuuint64_t>(kdim) * 2 * static_cast<cuuint64_t>(wrows)};
+    const cuuint32_t box[3] = {kBK, kBM, 1};
+    if (!encode_map(&ph.tmap_w, weights, 3, dims, strides, box)) return false;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim) * 2};
+    const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(plan.bn)};
+    if (!encode_map(&ph.tmap_x, act_in, 2, dims, strides, box)) return false;
+  }
+  ph.out = out;
+  ph.tickets = reinterpret_cast<int*>(base + (mode == 0 ? l.tickets0 : l.tickets1));
+  ph.partials = plan.split > 1 ? reinterpret_cast<float*>(base + (mode == 0 ? l.partials0 : l.partials1)) : nullptr;
+  ph.n_mb = mode == 0 ? F / kBM : H / kBM;
+  ph.ksteps = kdim / kBK;
+  ph.split = plan.split;
+  ph.out_ld = mode == 0 ? F : H;
+  ph.up_row = F;
+  ph.max_tiles = plan.max_tiles;
+  return true;
+}
+
+template <int BN>
+cudaError_t launch_fused_bn(const GemmParams& prm, int grid, cudaStream_t stream, bool pdl) {
+  return launch_mode_bn<2, BN>(prm, grid, stream, pdl);
+}
+
 }  // namespace
 
 size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down) {
-  const size_t a = partial_bytes(0, gate_up), b = partial_bytes(1, down);
-  return kCounterBytes + ticket_bytes(gate_up, down) + (a > b ? a : b);
+  return scratch_layout(gate_up, down).total;
 }
 
 size_t gemm_clear_bytes(const GemmPlan& gate_up, const GemmPlan& down) {
-  return kCounterBytes + ticket_bytes(gate_up, down);
+  return scratch_layout(gate_up, down).partials0;
 }
 
 cudaError_t clear_gemm_scratch(void* scratch, const GemmPlan& gate_up, const GemmPlan& down, cudaStream_t stream) {
@@ -690,39 +903,45 @@ cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down,
   const GemmPlan& plan = mode == 0 ? gate_up : down;
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
-  const int kdim = mode == 0 ? H : F;    // reduction length
-  const int wrows = mode == 0 ? 2 * F : H;
-  {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(wrows),
-                                static_cast<cuuint64_t>(E)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kdim) * 2,
-                                   static_cast<cuuint64_t>(kdim) * 2 * static_cast<cuuint64_t>(wrows)};
-    const cuuint32_t box[3] = {kBK, kBM, 1};
-    if (!encode_map(&prm.tmap_w, weights, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim) * 2};
-    const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(plan.bn)};
-    if (!encode_map(&prm.tmap_x, act_in, 2, dims, strides, box)) return cudaErrorInvalidValue;
-  }
   char* base = static_cast<char*>(scratch);
-  prm.counter = reinterpret_cast<int*>(base) + mode;
-  prm.tickets = reinterpret_cast<int*>(base + kCounterBytes);
-  prm.partials =
-      plan.split > 1 ? reinterpret_cast<float*>(base + kCounterBytes + ticket_bytes(gate_up, down)) : nullptr;
+  const ScratchLayout l = scratch_layout(gate_up, down);
+  if (!fill_phase(prm.ph[0], mode, plan, weights, act_in, rows, E, H, F, out, base, l)) return cudaErrorInvalidValue;
   prm.offsets = offsets;
-  prm.out = out;
+  prm.counter = reinterpret_cast<int*>(base) + mode;
+  prm.done = nullptr;
   prm.E = E;
   prm.rows = rows;
-  prm.n_mb = mode == 0 ? F / kBM : H / kBM;
-  prm.ksteps = kdim / kBK;
-  prm.split = plan.split;
-  prm.out_ld = mode == 0 ? F : H;
-  prm.up_row = F;
-  prm.max_tiles = plan.max_tiles;
+  prm.max_token_tiles = plan.max_token_tiles;
   return mode == 0 ? launch_mode<0>(plan.bn, prm, num_sms, stream, pdl)
                    : launch_mode<1>(plan.bn, prm, num_sms, stream, pdl);
+}
+
+bool fused_experts_supported(const GemmPlan& gate_up, const GemmPlan& down) {
+  return gate_up.bn == down.bn && gate_up.bn <= 64;
+}
+
+cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* w_gate_up,
+                                 const uint16_t* w_down, const uint16_t* x_perm, const int32_t* offsets, int rows,
+                                 int E, int H, int F, uint16_t* act, uint16_t* y_perm, void* scratch, int num_sms,
+                                 cudaStream_t stream, bool pdl) {
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  char* base = static_cast<char*>(scratch);
+  const ScratchLayout l = scratch_layout(gate_up, down);
+  if (!fill_phase(prm.ph[0], 0, gate_up, w_gate_up, x_perm, rows, E, H, F, act, base, l) ||
+      !fill_phase(prm.ph[1], 1, down, w_down, act, rows, E, H, F, y_perm, base, l))
+    return cudaErrorInvalidValue;
+  prm.offsets = offsets;
+  prm.counter = reinterpret_cast<int*>(base) + 2;
+  prm.done = reinterpret_cast<int*>(base + l.done);
+  prm.E = E;
+  prm.rows = rows;
+  prm.max_token_tiles = gate_up.max_token_tiles;
+  switch (gate_up.bn) {
+    case 16: return launch_fused_bn<16>(prm, num_sms, stream, pdl);
+    case 32: return launch_fused_bn<32>(prm, num_sms, stream, pdl);
+    default: return launch_fused_bn<64>(prm, num_sms, stream, pdl);
+  }
 }
 
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,

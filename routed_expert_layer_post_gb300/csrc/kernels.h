@@ -44,9 +44,10 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* z, int T, int K, 
 
 // ---- experts (experts.cu)
 struct GemmPlan {
-  int bn;         // token tile (MMA N): 16, 32, 64 or 128
-  int split;      // split-K factor (1 = no partial sums)
-  int max_tiles;  // upper bound on (expert, row-block, token-tile) tiles
+  int bn;               // token tile (MMA N): 16 .. 128 (256 for the down GEMM)
+  int split;            // split-K factor (1 = no partial sums)
+  int max_token_tiles;  // upper bound on (expert, token-tile) pairs
+  int max_tiles;        // upper bound on (expert, row-block, token-tile) tiles
 };
 // mode 0: gate/up + SwiGLU (weight rows 2F, reduction H); mode 1: down (rows H, reduction F)
 GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms);
@@ -56,6 +57,13 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms);
 size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down);
 cudaError_t clear_gemm_scratch(void* scratch, const GemmPlan& gate_up, const GemmPlan& down, cudaStream_t stream);
 size_t gemm_clear_bytes(const GemmPlan& gate_up, const GemmPlan& down);
+// Both GEMMs in one persistent launch (down units of a token tile wait for the
+// gate/up tiles that produce its rows); needs equal token tiles of <= 64.
+bool fused_experts_supported(const GemmPlan& gate_up, const GemmPlan& down);
+cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* w_gate_up,
+                                 const uint16_t* w_down, const uint16_t* x_perm, const int32_t* offsets, int rows,
+                                 int E, int H, int F, uint16_t* act, uint16_t* y_perm, void* scratch, int num_sms,
+                                 cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl = false);
