@@ -185,20 +185,40 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ["experts.cu", "ptx.cuh", "common.cuh", "kernels.h"]
+
+
+def kernel_source_digest() -> str:
+    """sha256 over the sources that define the expert GEMM kernels."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "routed_expert_layer_post_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profiled_traffic(kernel: str, workload: str):
-    """dram bytes per launch from a committed ncu summary, if one matches this kernel build."""
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or it was captured from other
+    kernel sources (its `source_sha256` line must match the current build)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
+    fields = {}
     for line in text.splitlines():
-        if line.strip().startswith("dram_bytes_per_launch:"):
-            try:
-                return float(line.split(":", 1)[1].split()[0])
-            except ValueError:
-                return None
-    return None
+        line = line.strip().strip("`")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().split()[0] if v.strip() else ""
+    if fields.get("source_sha256") != kernel_source_digest():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ---------------------------------------------------------------- CPU oracle timing
