@@ -392,10 +392,30 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
   record(dbg, 0, s);
   // every kernel of the layer is launched with programmatic dependent launch
   const bool pdl = true;
-  // the boundary also zeroes the router's ticket (used when router and top-k share a launch)
   int* router_ticket = reinterpret_cast<int*>(base + L.router_ticket);
-  cudaError_t e =
-      beam::launch_boundary(h, x, wt->w_post, wt->w_pre, T, H, cfg->eps, n, h_out, z, s, pdl, router_ticket);
+  const beam::GemmPlan p0 = beam::plan_gemm(0, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  const beam::GemmPlan p1 = beam::plan_gemm(1, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  char* gemm_scratch = base + L.experts + experts_ws(cfg, T, d.sms).gemm;
+  cudaError_t e;
+  if (beam::route_decode_supported(T, H, cfg->num_experts, cfg->num_groups, cfg->topk)) {
+    // decode sizes: boundary, router, top-k, permutation and the GEMM scratch
+    // clear in one launch (the stage events of router and permutation are empty)
+    e = beam::launch_route_decode(h, x, wt->w_post, wt->w_pre, wt->router_w, wt->bias, T, H, cfg->num_experts,
+                                  cfg->num_groups, cfg->topk_groups, cfg->topk, cfg->routed_scale, cfg->eps, n,
+                                  h_out, z, logits, ids, w, offsets, perm, inv, x_perm, router_ticket, gemm_scratch,
+                                  beam::gemm_clear_bytes(p0, p1), s, pdl);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    record(dbg, 1, s);
+    record(dbg, 2, s);
+    launches += launch_counter();
+    launch_counter() = 0;
+    st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
+                     dbg, pdl, /*cleared=*/true);
+    launch_counter() += launches;
+    return st;
+  }
+  // the boundary also zeroes the router's ticket (used when router and top-k share a launch)
+  e = beam::launch_boundary(h, x, wt->w_post, wt->w_pre, T, H, cfg->eps, n, h_out, z, s, pdl, router_ticket);
   if (e != cudaSuccess) return BEAM_ERR_CUDA;
   record(dbg, 1, s);
   launches += launch_counter();
@@ -414,9 +434,6 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
   }
   record(dbg, 2, s);
   // the permutation also zeroes the experts' counters and tickets
-  const beam::GemmPlan p0 = beam::plan_gemm(0, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
-  const beam::GemmPlan p1 = beam::plan_gemm(1, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
-  char* gemm_scratch = base + L.experts + experts_ws(cfg, T, d.sms).gemm;
   e = beam::launch_permute(ids, z, T, cfg->topk, cfg->num_experts, H, offsets, perm, inv, x_perm,
                            base + L.perm_scratch, s, pdl, gemm_scratch, beam::gemm_clear_bytes(p0, p1));
   if (e != cudaSuccess) return BEAM_ERR_CUDA;

@@ -353,11 +353,38 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         dep_ready = true;
       };
       int ready_gtt = -1;  // MODE 2: the last token tile whose gate/up rows were seen complete
+      // MODE 2: a down unit whose activation rows are not complete yet still
+      // streams its weight tiles; its activation loads wait here (token tile
+      // pend_gtt, first deferred unit pend_seq0) until the gate/up units of
+      // that tile are done, the ring is full, or the unit queue would block
+      int pend_gtt = -1, pend_seq0 = 0;
+      bool pend_two[C::kStages];
+      auto release_down = [&]() -> bool {
+        if (!wait_counter(p.done + pend_gtt, p.ph[0].n_mb, abort_flag, 8)) return false;
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
+        for (int i = 0; i < npend; ++i) {
+          uint8_t* st = tiles + pend_stage[i] * C::kStageBytes + C::kNAcc * kTileABytes;
+          ptx::tma_load_2d(st, &p.ph[1].tmap_x, &full[pend_stage[i]], pend_k[i] * kBK, pend_row[i], pol_x);
+          if (pend_two[i])
+            ptx::tma_load_2d(st + C::kTileBBytes, &p.ph[1].tmap_x, &full[pend_stage[i]], (pend_k[i] + 1) * kBK,
+                             pend_row[i], pol_x);
+        }
+        npend = 0;
+        ready_gtt = pend_gtt;
+        return true;
+      };
       int u_next = static_cast<int>(blockIdx.x);
       for (int seq = 0;; ++seq) {
         int u = u_next;
         if (u >= n_units || !ok) u = -1;
         if (u < 0 && !dep_ready) release_pending();
+        if (MODE == 2 && npend > 0 && ok && (u < 0 || seq - pend_seq0 >= kQueue - 1)) {
+          // the MMA warp may be waiting on a deferred stage: it frees no queue slot until it gets it
+          if (!release_down()) {
+            ok = false;
+            u = -1;
+          }
+        }
         const int slot = seq % kQueue;
         if (!wait_bar(&qempty[slot], ((seq / kQueue) & 1) ^ 1u, abort_flag, 5, kTimeoutNs)) {
           ok = false;
@@ -375,19 +402,40 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const uint32_t stage_bytes = nacc * kTileABytes + C::kTileBBytes;
         const int k0 = w.s * ph.ksteps / ph.split, k1 = (w.s + 1) * ph.ksteps / ph.split;
         const int row0 = s_off[w.e] + w.tt * BN;
-        if (MODE == 2 && w.phase == 1 && w.gtt != ready_gtt) {
+        bool defer = false;
+        if (MODE == 2 && w.phase == 1) {
           // this token tile's rows of `act` come from gate/up units held by
-          // running CTAs (all gate/up units are handed out before any down unit)
-          if (!wait_counter(p.done + w.gtt, p.ph[0].n_mb, abort_flag, 8)) {
-            ok = false;
-            continue;
+          // running CTAs (all gate/up units are handed out before any down
+          // unit). Deferred stages are always the newest in the ring: a unit
+          // of another token tile first releases them.
+          if (npend > 0 && (pend_gtt != w.gtt || ld_acquire(p.done + pend_gtt) >= p.ph[0].n_mb)) {
+            if (!release_down()) {
+              ok = false;
+              continue;
+            }
           }
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
-          ready_gtt = w.gtt;
+          if (w.gtt != ready_gtt) {
+            if (npend == 0 && ld_acquire(p.done + w.gtt) >= p.ph[0].n_mb) {
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              ready_gtt = w.gtt;
+            } else {
+              if (npend == 0) pend_seq0 = seq;
+              pend_gtt = w.gtt;
+              defer = true;
+            }
+          }
         }
         // k-steps per stage: 1, or 2 for down units of the fused launch
         const int kps = (MODE == 2 && kind == 1) ? 2 : 1;
         for (int k = k0; k < k1; k += kps) {
+          if (MODE == 2 && npend == C::kStages) {
+            // every stage holds a deferred tile: the MMA needs the activations now
+            if (!release_down()) {
+              ok = false;
+              break;
+            }
+            defer = false;
+          }
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, 1, kTimeoutNs)) {
             ok = false;
             break;
@@ -397,11 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             const bool two = k + 1 < k1;
             ptx::mbar_arrive_expect_tx(&full[stage], (two ? 2u : 1u) * (kTileABytes + C::kTileBBytes));
             ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e, pol_w);
-            ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &ph.tmap_x, &full[stage], k * kBK, row0, pol_x);
-            if (two) {
+            if (two)
               ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], (k + 1) * kBK, w.mb * kBM, w.e, pol_w);
-              ptx::tma_load_2d(st + C::kNAcc * kTileABytes + C::kTileBBytes, &ph.tmap_x, &full[stage],
-                               (k + 1) * kBK, row0, pol_x);
+            if (defer) {
+              pend_stage[npend] = stage;
+              pend_k[npend] = k;
+              pend_row[npend] = row0;
+              pend_two[npend] = two;
+              ++npend;
+            } else {
+              ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &ph.tmap_x, &full[stage], k * kBK, row0, pol_x);
+              if (two)
+                ptx::tma_load_2d(st + C::kNAcc * kTileABytes + C::kTileBBytes, &ph.tmap_x, &full[stage],
+                                 (k + 1) * kBK, row0, pol_x);
             }
             ++issued;
             if (++stage == C::kStages) {

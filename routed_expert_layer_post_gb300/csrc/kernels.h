@@ -34,6 +34,19 @@ cudaError_t launch_router_topk_fused(const uint16_t* z, const float* W, const fl
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int G, int TG, int K, float scale,
                         int32_t* ids, float* w, cudaStream_t stream, bool pdl = false);
 
+// ---- decode routing (route_decode.cu)
+// Boundary -> router -> top-k -> permutation -> row gather in one launch, and
+// `clear_bytes` of `clear` zeroed (the experts' counters and tickets), for
+// T <= 8 with 256 experts in 8 groups. `ticket` is zeroed by a memset before
+// the launch and left zero.
+bool route_decode_supported(int T, int H, int E, int G, int K);
+cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
+                                const float* W, const float* bias, int T, int H, int E, int G, int TG, int K,
+                                float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
+                                int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
+                                uint16_t* x_perm, int* ticket, void* clear, size_t clear_bytes, cudaStream_t stream,
+                                bool pdl);
+
 // ---- permutation (permute.cu)
 size_t permute_scratch_bytes(int T, int K, int E);
 // `clear` (optional): bytes zeroed before the permutation completes (the

@@ -1,0 +1,194 @@
+// Device arithmetic of the sandwich-norm boundary, shared by the boundary
+// kernel and the fused decode routing kernel: double-float sums of squares,
+// the per-token normaliser, and bf16 rounding of the three outputs with a
+// rigorous fp32 fast path and an exact double-float fallback (see
+// boundary.cu for the numerics).
+#pragma once
+
+#include "common.cuh"
+
+#include <cmath>
+
+namespace beam {
+namespace norm {
+
+struct F2 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ F2 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+  return {s, e};
+}
+
+__device__ __forceinline__ void acc_add(F2& acc, float v) {
+  const F2 t = two_sum(acc.hi, v);
+  acc.hi = t.hi;
+  acc.lo = __fadd_rn(acc.lo, t.lo);
+}
+
+// symmetric in its arguments, so butterfly reductions agree bit for bit on every lane
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const F2 t = two_sum(a.hi, b.hi);
+  const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), t.lo);
+  const float hi = __fadd_rn(t.hi, lo);
+  return {hi, __fsub_rn(lo, __fsub_rn(hi, t.hi))};
+}
+
+__device__ __forceinline__ F2 warp_sum_f2(F2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    F2 w;
+    w.hi = __shfl_xor_sync(kFullMask, v.hi, o);
+    w.lo = __shfl_xor_sync(kFullMask, v.lo, o);
+    v = f2_add(v, w);
+  }
+  return v;
+}
+
+// 1/sqrt(sum/H + eps) as an fp32 pair, from a double-float sum of squares.
+// GB300 runs fp64 at a small fraction of the fp32 rate, so one thread per
+// token evaluates this and the result is broadcast.
+__device__ __forceinline__ F2 rsqrt_mean(F2 sum, double inv_h, double eps) {
+  const double ms = (static_cast<double>(sum.hi) + static_cast<double>(sum.lo)) * inv_h + eps;
+  const double r = 1.0 / sqrt(ms);
+  const float hi = static_cast<float>(r);
+  return {hi, static_cast<float>(r - static_cast<double>(hi))};
+}
+
+// bf16 bits of the exact value hi + lo, where |lo| <= half an fp32 ulp of hi
+__device__ __forceinline__ uint32_t round_pair(float hi, float lo) {
+  const uint32_t b = __float_as_uint(hi);
+  if ((b & 0xffffu) == 0x8000u && lo != 0.0f) {
+    const bool grow = (lo > 0.0f) == (hi > 0.0f);
+    return (b >> 16) + (grow ? 1u : 0u);
+  }
+  return f2bf(hi);
+}
+
+// bf16 bits of a * b * r with a, b bf16 values (a * b exact in fp32) and r a pair
+__device__ __forceinline__ uint32_t scaled_bf16(float a, float b, const F2& r) {
+  const float ab = __fmul_rn(a, b);
+  const float p = __fmul_rn(ab, r.hi);
+  float pe = fmaf(ab, r.hi, -p);
+  pe = fmaf(ab, r.lo, pe);
+  const float hi = __fadd_rn(p, pe);
+  return round_pair(hi, __fsub_rn(pe, __fsub_rn(hi, p)));
+}
+
+// Coefficients of the residual add as fp32 pairs: sqrt(n-1) = cm_hi + cm_lo,
+// 1/sqrt(n) = c_hi + c_lo.
+struct ResidualCoef {
+  float cm_hi, cm_lo, c_hi, c_lo;
+};
+
+// bf16 bits of (sqrt(n-1) h + y) / sqrt(n)
+__device__ __forceinline__ uint32_t residual_bf16(float h, float y, const ResidualCoef& k) {
+  const float p = __fmul_rn(k.cm_hi, h);
+  float pe = fmaf(k.cm_hi, h, -p);
+  pe = fmaf(k.cm_lo, h, pe);
+  const F2 s = two_sum(p, y);
+  float u_lo = __fadd_rn(s.lo, pe);
+  const float u_hi = __fadd_rn(s.hi, u_lo);
+  u_lo = __fsub_rn(u_lo, __fsub_rn(u_hi, s.hi));
+  const float v = __fmul_rn(u_hi, k.c_hi);
+  float ve = fmaf(u_hi, k.c_hi, -v);
+  ve = fmaf(u_hi, k.c_lo, ve);
+  ve = fmaf(u_lo, k.c_hi, ve);
+  const float v_hi = __fadd_rn(v, ve);
+  return round_pair(v_hi, __fsub_rn(ve, __fsub_rn(v_hi, v)));
+}
+
+__device__ __forceinline__ void acc_squares(F2& acc, const uint4& v) {
+  float f[8];
+  unpack8(v, f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc_add(acc, __fmul_rn(f[i], f[i]));  // exact square of a bf16 value
+}
+
+// Adaptive precision: the plain fp32 value v is used when every value within
+// its error bound e rounds to the same bf16 number (the usual case); only
+// values whose interval [v - e, v + e] straddles a rounding midpoint take the
+// exact double-float path above. The bounds are deliberately loose (about
+// four times the worst-case fp32 error), so the fast path never decides a
+// case the exact path would decide differently.
+__device__ __forceinline__ bool rounds_alike(float v, float e) {
+  return f2bf(__fsub_rn(v, e)) == f2bf(__fadd_rn(v, e));
+}
+
+// bf16(a * b * r), a and b bf16 values, r a pair with |r.lo| <= 2^-24 |r.hi|
+__device__ __forceinline__ uint32_t scaled_bf16_fast(float a, float b, const F2& r) {
+  const float v = __fmul_rn(__fmul_rn(a, b), r.hi);  // a * b is exact
+  if (rounds_alike(v, fabsf(v) * 0x1p-21f)) return f2bf(v);
+  return scaled_bf16(a, b, r);
+}
+
+// bf16((sqrt(n-1) h + y) / sqrt(n)); the error of the fp32 evaluation is
+// bounded by a few ulps of c * (|sqrt(n-1) h| + |y|), which covers cancellation
+__device__ __forceinline__ uint32_t residual_bf16_fast(float h, float y, const ResidualCoef& k) {
+  const float ch = __fmul_rn(k.cm_hi, h);
+  const float v = __fmul_rn(fmaf(k.cm_hi, h, y), k.c_hi);
+  const float e = __fmul_rn(__fadd_rn(fabsf(ch), fabsf(y)), k.c_hi) * 0x1p-20f;
+  if (rounds_alike(v, e)) return f2bf(v);
+  return residual_bf16(h, y, k);
+}
+
+// y and h' for one 8-element chunk; returns h' packed, accumulates its squares
+__device__ __forceinline__ uint4 chunk_residual(const uint4& xv, const uint4& hv, const uint4& wv, const F2& r,
+                                                const ResidualCoef& coef, F2& acc) {
+  float fx[8], fh[8], fw[8], hn[8];
+  unpack8(xv, fx);
+  unpack8(hv, fh);
+  unpack8(wv, fw);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float y = __uint_as_float(scaled_bf16_fast(fx[i], fw[i], r) << 16);
+    hn[i] = __uint_as_float(residual_bf16_fast(fh[i], y, coef) << 16);
+    acc_add(acc, __fmul_rn(hn[i], hn[i]));
+  }
+  return pack8(hn);
+}
+
+__device__ __forceinline__ uint4 chunk_scale(const uint4& hv, const uint4& wv, const F2& r) {
+  float fh[8], fw[8];
+  unpack8(hv, fh);
+  unpack8(wv, fw);
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = scaled_bf16_fast(fh[i], fw[i], r);
+  return make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16), o[6] | (o[7] << 16));
+}
+
+// block-wide sum of squares -> 1/sqrt(mean + eps), evaluated by thread 0;
+// red needs 33 entries
+__device__ __forceinline__ F2 block_rsqrt_mean(F2 v, F2* red, int nwarps, double inv_h, double eps) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  v = warp_sum_f2(v);
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    F2 t = (lane < nwarps) ? red[lane] : F2{0.f, 0.f};
+    t = warp_sum_f2(t);
+    if (lane == 0) red[32] = rsqrt_mean(t, inv_h, eps);
+  }
+  __syncthreads();
+  const F2 r = red[32];
+  __syncthreads();  // red is reused by the next reduction
+  return r;
+}
+
+// coefficients of the residual add for boundary index n
+inline ResidualCoef residual_coef(int n) {
+  const double cm = std::sqrt(static_cast<double>(n - 1)), c = 1.0 / std::sqrt(static_cast<double>(n));
+  ResidualCoef coef;
+  coef.cm_hi = static_cast<float>(cm);
+  coef.cm_lo = static_cast<float>(cm - static_cast<double>(coef.cm_hi));
+  coef.c_hi = static_cast<float>(c);
+  coef.c_lo = static_cast<float>(c - static_cast<double>(coef.c_hi));
+  return coef;
+}
+
+}  // namespace norm
+}  // namespace beam

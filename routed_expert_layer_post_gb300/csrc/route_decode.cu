@@ -1,0 +1,224 @@
+// Decode-size routing in one launch: boundary -> FP32 router -> group top-k
+// -> permutation -> row gather, for up to kMaxT tokens with Beam's expert
+// layout (256 experts in 8 groups).
+//
+// Same arithmetic as the separate kernels (boundary.cu, router.cu,
+// permute.cu; their page citations apply): the sandwich-norm boundary with
+// bf16 rounding points, FP32 router logits with fp32 FMA, sigmoid + bias,
+// top-2-sum group scores, TG groups, K experts, weights * routed_scale, and
+// the stable (expert, token) order.
+//
+// One block per expert, one thread per 8 hidden elements. At decode the
+// token rows are ~10 KB, so every block recomputes the boundary for the
+// tokens (redundant but cheap, and it removes a launch and a round trip of
+// z), then dots z with its expert's router row. The last block to finish
+// (ticket counter, zeroed by the host before the launch) writes h' and z, runs
+// the top-k for every token and the permutation of the T*K pairs, copies the
+// permuted rows from the z it holds in registers, and clears the expert
+// GEMMs' counters and tickets. Only that block writes h': h' may alias h, and
+// by then every block has read h.
+#include "common.cuh"
+#include "kernels.h"
+#include "norm_math.cuh"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace beam {
+
+namespace {
+
+using namespace norm;
+
+constexpr int kMaxT = 8;
+constexpr int kMaxPairs = 64;
+constexpr int kMaxThreads = 640;  // H <= 5120
+
+// TMAX: token capacity of the register arrays. Up to two tokens, two blocks
+// fit on an SM, so all 256 expert blocks are resident at once on 152 SMs.
+template <int TMAX>
+__global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
+    route_decode_kernel(const uint4* h, const uint4* __restrict__ x, const uint4* __restrict__ w_post,
+                        const uint4* __restrict__ w_pre, const float* __restrict__ W, const float* __restrict__ bias,
+                        int T, int E, int G, int TG, int K, float scale, double inv_h, double eps, ResidualCoef coef,
+                        uint4* h_out, uint4* __restrict__ z_out, float* __restrict__ logits,
+                        int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_perm, uint4* __restrict__ x_perm,
+                        int* ticket, int* __restrict__ clear, int clear_ints) {
+  __shared__ F2 red[33];
+  __shared__ float fred[32];
+  __shared__ int hist[256];
+  __shared__ int s_pos[kMaxPairs];
+  __shared__ int s_ids[kMaxPairs];
+  __shared__ int s_last;
+  const int c = threadIdx.x;  // 8-element chunk owned by this thread
+  const int nc = blockDim.x;
+  const int nwarps = nc >> 5;
+  const int lane = c & 31, warp = c >> 5;
+  const int e = blockIdx.x;
+
+  // constants first: they do not depend on the previous kernel
+  const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * nc * 8);
+  const float4 wa = __ldg(wrow + 2 * c), wb = __ldg(wrow + 2 * c + 1);
+  const uint4 wp = w_post[c];
+  const uint4 wq = w_pre[c];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+
+  uint4 hc[TMAX], zc[TMAX];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    hc[t] = make_uint4(0u, 0u, 0u, 0u);
+    zc[t] = hc[t];
+    if (t < T) {
+      const size_t idx = static_cast<size_t>(t) * nc + c;
+      const uint4 xv = x[idx];
+      const uint4 hv = h[idx];
+      F2 acc{0.f, 0.f};
+      acc_squares(acc, xv);
+      const F2 r = block_rsqrt_mean(acc, red, nwarps, inv_h, eps);
+      F2 acc2{0.f, 0.f};
+      hc[t] = chunk_residual(xv, hv, wp, r, coef, acc2);
+      const F2 r2 = block_rsqrt_mean(acc2, red, nwarps, inv_h, eps);
+      zc[t] = chunk_scale(hc[t], wq, r2);
+      // router logit of expert e: z . W_r[e] in fp32 FMA, fixed reduction order
+      float zf[8];
+      unpack8(zc[t], zf);
+      float dot = 0.f;
+      dot = fmaf(zf[0], wa.x, dot);
+      dot = fmaf(zf[1], wa.y, dot);
+      dot = fmaf(zf[2], wa.z, dot);
+      dot = fmaf(zf[3], wa.w, dot);
+      dot = fmaf(zf[4], wb.x, dot);
+      dot = fmaf(zf[5], wb.y, dot);
+      dot = fmaf(zf[6], wb.z, dot);
+      dot = fmaf(zf[7], wb.w, dot);
+      dot = warp_sum(dot);
+      if (lane == 0) fred[warp] = dot;
+      __syncthreads();
+      if (warp == 0) {
+        const float s = warp_sum(lane < nwarps ? fred[lane] : 0.f);
+        if (lane == 0) logits[static_cast<size_t>(t) * E + e] = s;
+      }
+      __syncthreads();
+    }
+  }
+
+  // the last block to finish sees every expert's logits
+  __threadfence();
+  __syncthreads();
+  if (c == 0) s_last = (atomicAdd(ticket, 1) == E - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    if (t < T) {
+      const size_t idx = static_cast<size_t>(t) * nc + c;
+      h_out[idx] = hc[t];
+      z_out[idx] = zc[t];
+    }
+  }
+
+  for (int t = warp; t < T; t += nwarps)
+    topk_lanes_token<8, 4>(logits, bias, t, G, TG, K, scale, ids, wout, s_ids + t * K);
+  __syncthreads();
+
+  const int pairs = T * K;
+  if (warp == 0) {
+    // counts, exclusive scan over experts, stable positions in (expert, pair) order
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    int my_e[2], my_i[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      my_i[q] = lane + 32 * q;
+      my_e[q] = my_i[q] < pairs ? s_ids[my_i[q]] : -1;
+      if (my_e[q] >= E) my_e[q] = -1;  // no valid choice (non-finite scores): dropped
+      if (my_e[q] >= 0) atomicAdd(&hist[my_e[q]], 1);
+    }
+    __syncwarp();
+    const int per_lane = (E + 31) / 32;
+    int local = 0;
+    for (int j = 0; j < per_lane; ++j) {
+      const int ee = lane * per_lane + j;
+      if (ee < E) local += hist[ee];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    __syncwarp();
+    for (int j = 0; j < per_lane; ++j) {
+      const int ee = lane * per_lane + j;
+      if (ee < E) {
+        const int cnt = hist[ee];
+        offsets[ee] = run;
+        hist[ee] = run;  // becomes the expert's first position
+        run += cnt;
+      }
+    }
+    if (lane == 31) offsets[E] = incl;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (my_i[q] < pairs) {
+        int pos = -1;
+        if (my_e[q] >= 0) {
+          int before = 0;  // earlier pairs with the same expert
+          for (int j = 0; j < my_i[q]; ++j) before += (s_ids[j] == my_e[q]);
+          pos = hist[my_e[q]] + before;
+          perm_token[pos] = my_i[q] / K;
+        }
+        s_pos[my_i[q]] = pos;
+        inv_perm[my_i[q]] = pos;
+      }
+    }
+  }
+  __syncthreads();
+  // permuted rows straight from the z this block holds
+  for (int i = 0; i < pairs; ++i) {
+    if (s_pos[i] < 0) continue;
+    const int t = i / K;
+    uint4 v = zc[0];
+#pragma unroll
+    for (int tt = 1; tt < TMAX; ++tt)
+      if (tt == t) v = zc[tt];
+    x_perm[static_cast<size_t>(s_pos[i]) * nc + c] = v;
+  }
+  for (int j = c; j < clear_ints; j += nc) clear[j] = 0;
+  if (c == 0) *ticket = 0;
+}
+
+}  // namespace
+
+bool route_decode_supported(int T, int H, int E, int G, int K) {
+  return T >= 1 && T <= kMaxT && E == 256 && G == 8 && T * K <= kMaxPairs && H % 256 == 0 &&
+         H / 8 <= kMaxThreads;
+}
+
+cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
+                                const float* W, const float* bias, int T, int H, int E, int G, int TG, int K,
+                                float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
+                                int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
+                                uint16_t* x_perm, int* ticket, void* clear, size_t clear_bytes, cudaStream_t stream,
+                                bool pdl) {
+  cudaError_t err = cudaMemsetAsync(ticket, 0, sizeof(int), stream);
+  if (err != cudaSuccess) return err;
+  const ResidualCoef coef = norm::residual_coef(n);
+  auto kernel = T <= 1 ? route_decode_kernel<1> : T <= 2 ? route_decode_kernel<2>
+              : T <= 4 ? route_decode_kernel<4> : route_decode_kernel<8>;
+  err = launch_kernel(kernel, dim3(E), dim3(H / 8), 0, stream, pdl, reinterpret_cast<const uint4*>(h),
+                      reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(w_post),
+                      reinterpret_cast<const uint4*>(w_pre), W, bias, T, E, G, TG, K, scale, 1.0 / H,
+                      static_cast<double>(eps), coef, reinterpret_cast<uint4*>(h_out), reinterpret_cast<uint4*>(z_out),
+                      logits, ids, w, offsets, perm_token, inv_perm, reinterpret_cast<uint4*>(x_perm), ticket,
+                      static_cast<int*>(clear), static_cast<int>(clear_bytes / sizeof(int)));
+  ++launch_counter();
+  return err;
+}
+
+}  // namespace beam
