@@ -5,6 +5,7 @@
 #include "../../include/beam.h"
 #include "kernels.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -87,12 +88,17 @@ constexpr int kPlanSms = 152;
 ExpertsWs experts_ws(const beam_moe_config_t* c, int T, int sms) {
   ExpertsWs w{};
   const size_t rows = static_cast<size_t>(T) * c->topk;
-  const beam::GemmPlan p0 = beam::plan_gemm(0, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
-  const beam::GemmPlan p1 = beam::plan_gemm(1, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  // scratch for the experts stage's plans and for the separate gate/up and
+  // down entry points' plans (which may split differently)
+  beam::GemmPlan p0, p1;
+  beam::plan_experts(T, c->topk, c->num_experts, c->hidden, c->d_ff, sms, &p0, &p1);
+  const beam::GemmPlan q0 = beam::plan_gemm(0, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  const beam::GemmPlan q1 = beam::plan_gemm(1, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  const size_t scratch = std::max(beam::gemm_scratch_bytes(p0, p1), beam::gemm_scratch_bytes(q0, q1));
   w.act = 0;
   w.y_perm = align_up(w.act + rows * c->d_ff * 2);
   w.gemm = align_up(w.y_perm + rows * c->hidden * 2);
-  w.total = align_up(w.gemm + beam::gemm_scratch_bytes(p0, p1));
+  w.total = align_up(w.gemm + scratch);
   return w;
 }
 
@@ -141,8 +147,8 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
   uint16_t* act = reinterpret_cast<uint16_t*>(ws + w.act);
   uint16_t* y_perm = reinterpret_cast<uint16_t*>(ws + w.y_perm);
   void* g = ws + w.gemm;
-  const beam::GemmPlan p0 = beam::plan_gemm(0, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
-  const beam::GemmPlan p1 = beam::plan_gemm(1, T, c->topk, c->num_experts, c->hidden, c->d_ff, sms);
+  beam::GemmPlan p0, p1;
+  beam::plan_experts(T, c->topk, c->num_experts, c->hidden, c->d_ff, sms, &p0, &p1);
   // unit counters and split-K tickets start at zero (one memset for both GEMMs)
   cudaError_t e = cudaSuccess;
   if (!cleared && (e = beam::clear_gemm_scratch(g, p0, p1, s)) != cudaSuccess) return BEAM_ERR_CUDA;
@@ -393,8 +399,8 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
   // every kernel of the layer is launched with programmatic dependent launch
   const bool pdl = true;
   int* router_ticket = reinterpret_cast<int*>(base + L.router_ticket);
-  const beam::GemmPlan p0 = beam::plan_gemm(0, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
-  const beam::GemmPlan p1 = beam::plan_gemm(1, T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms);
+  beam::GemmPlan p0, p1;
+  beam::plan_experts(T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms, &p0, &p1);
   char* gemm_scratch = base + L.experts + experts_ws(cfg, T, d.sms).gemm;
   cudaError_t e;
   if (beam::route_decode_supported(T, H, cfg->num_experts, cfg->num_groups, cfg->topk)) {

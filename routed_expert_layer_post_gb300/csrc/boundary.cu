@@ -50,7 +50,7 @@ using namespace norm;
 // ------------------------------------------------------------------ block per token
 __global__ void __launch_bounds__(1024)
     boundary_block_kernel(const uint4* h, const uint4* __restrict__ x, const uint4* __restrict__ w_post,
-                          const uint4* __restrict__ w_pre, int nc, double inv_h, double eps, ResidualCoef coef,
+                          const uint4* __restrict__ w_pre, int nc, F2 inv_h, float eps, ResidualCoef coef,
                           uint4* h_out, uint4* __restrict__ z_out, int* zero_slot) {
   __shared__ F2 red[33];
   ptx::griddep_wait();  // inputs come from the previous kernel
@@ -81,7 +81,7 @@ cudaError_t launch_boundary(const uint16_t* h, const uint16_t* x, const uint16_t
                             int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out, cudaStream_t stream,
                             bool pdl, int* zero_slot) {
   const ResidualCoef coef = residual_coef(n);
-  const double inv_h = 1.0 / H, e = static_cast<double>(eps);
+  const F2 inv_h = inv_hidden(H);
   const uint4* hp = reinterpret_cast<const uint4*>(h);
   const uint4* xp = reinterpret_cast<const uint4*>(x);
   const uint4* wp = reinterpret_cast<const uint4*>(w_post);
@@ -89,7 +89,7 @@ cudaError_t launch_boundary(const uint16_t* h, const uint16_t* x, const uint16_t
   uint4* ho = reinterpret_cast<uint4*>(h_out);
   uint4* zo = reinterpret_cast<uint4*>(z_out);
   const cudaError_t err = launch_kernel(boundary_block_kernel, dim3(T), dim3(H / 8), 0, stream, pdl, hp, xp, wp, wq,
-                                        H / 8, inv_h, e, coef, ho, zo, zero_slot);
+                                        H / 8, inv_h, eps, coef, ho, zo, zero_slot);
   ++launch_counter();
   return err;
 }

@@ -44,7 +44,11 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int kThreads = 192;
+// warp 0: scheduler + TMA producer; warp 1: MMA issuer; warps 2-5 and 6-9:
+// two epilogue groups taking alternate units (each group covers the four
+// TMEM lane quarters), so one group's split-K round trips overlap the other's
+constexpr int kThreads = 320;
+constexpr int kEpiGroups = 2;
 constexpr int kBM = 128;                     // weight rows per tile (MMA M)
 constexpr int kBK = 64;                      // reduction elements per stage: 128 bytes of bf16
 constexpr int kTileABytes = kBM * kBK * 2;   // 16 KB
@@ -104,7 +108,7 @@ struct Cfg {
   static constexpr int kAccCols = kNAcc * BN;
   // two accumulator buffers in TMEM: the epilogue of one tile overlaps the
   // MMAs of the next (four were measured slower at decode)
-  static constexpr int kAccBufs = 2;
+  static constexpr int kAccBufs = 2;  // one per epilogue group
   static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
@@ -130,6 +134,19 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
       }
     }
   }
+}
+
+// Split-K ticket: one atomic with acquire-release semantics at GPU scope (the
+// caller's partial stores, ordered before it by a CTA barrier, are released
+// with it; the last arriver acquires the other CTAs' partials).
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void red_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -228,9 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   uint64_t* qempty = qfull + kQueue;
   uint64_t* drain = qempty + kQueue;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  // [0] abort, [1] last arriver, [3] current unit (epilogue broadcast)
+  // [0] abort; per epilogue group g: [4g+1] last arriver, [4g+3] current unit
   int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_queue = s_flags + 4;
+  int* s_queue = s_flags + 8;
   int* s_off = s_queue + kQueue;
   int* s_ntt = s_off + kMaxE + 1;
   int* s_ttstart = s_ntt + kMaxE;
@@ -251,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       ptx::mbar_init(&qempty[q], 2);  // released by the MMA thread and the epilogue leader
     }
     ptx::mbar_init(drain, 1);
-    for (int i = 0; i < 4; ++i) s_flags[i] = 0;
+    for (int i = 0; i < 8; ++i) s_flags[i] = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -392,7 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         }
         s_queue[slot] = u;
         ptx::mbar_arrive(&qfull[slot]);
-        if (u < 0) break;
+        if (u < 0) {
+          // the epilogue group that would take the next unit also needs the stop mark
+          const int s2 = (seq + 1) % kQueue;
+          wait_bar(&qempty[s2], (((seq + 1) / kQueue) & 1) ^ 1u, abort_flag, 5, kTimeoutNs);
+          s_queue[s2] = -1;
+          ptx::mbar_arrive(&qfull[s2]);
+          break;
+        }
         // ask for the following unit now: the atomic's round trip overlaps this unit's loads
         u_next = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
         const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
@@ -569,14 +593,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2-5)
-    const int sub = warp & 3;  // TMEM lane quarter this warp may access
+    static_assert(C::kAccBufs == kEpiGroups, "epilogue group g owns accumulator buffer g");
+    const int eg = (warp - 2) >> 2;  // epilogue group: units eg, eg + 2, ...
+    const int sub = warp & 3;        // TMEM lane quarter this warp may access
     const int m = sub * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
-    const bool leader = (warp == 2 && lane == 0);
+    const bool leader = (warp == 2 + 4 * eg && lane == 0);
+    const uint32_t bar_id = 1 + eg;
+    int* g_flags = s_flags + 4 * eg;
     if (MODE == 1) ptx::griddep_wait();  // tickets and partial sums were last used by the previous kernel
-    int acc = 0;
+    const int acc = eg;
     uint32_t acc_phase = 0;
-    for (int seq = 0;; ++seq) {
+    for (int seq = eg;; seq += kEpiGroups) {
       if (leader) {
         const int slot = seq % kQueue;
         int u = -1;
@@ -584,11 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         ptx::mbar_arrive(&qempty[slot]);
         int ready = 0;
         if (u >= 0) ready = wait_bar(&tfull[acc], acc_phase, abort_flag, 4, kTimeoutNs) ? 1 : 0;
-        s_flags[3] = ready ? u : -1;
+        g_flags[3] = ready ? u : -1;
       }
-      ptx::named_bar_sync(1, 128);
-      const int u = *reinterpret_cast<volatile int*>(&s_flags[3]);
-      ptx::named_bar_sync(1, 128);
+      ptx::named_bar_sync(bar_id, 128);
+      const int u = *reinterpret_cast<volatile int*>(&g_flags[3]);
+      ptx::named_bar_sync(bar_id, 128);
       if (u < 0) break;
       ptx::tc_fence_after();
       const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
@@ -600,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const int col = w.mb * kBM + m;
       const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * C::kAccCols);
       bool tile_done = false;  // this unit completed its tile's outputs
+      bool released = false;   // the accumulator was already handed back
       if (ph.split == 1) {
         for (int c0 = 0; c0 < valid; c0 += 16) {
           uint32_t r[2][16];
@@ -616,6 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         }
         tile_done = true;
       } else {
+        // The accumulator is read once, stored as this split's partial, and
+        // handed back to the MMA warp at once: the ticket round trip and the
+        // final sum (which reads every split's partial, this one included,
+        // from global memory) no longer hold the tensor memory.
         const size_t slot_elems = static_cast<size_t>(nacc * BN) * kBM;
         float* mine = ph.partials + (static_cast<size_t>(w.tile) * ph.split + w.s) * slot_elems;
         for (int c0 = 0; c0 < valid; c0 += 16) {
@@ -631,27 +664,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               for (int j = 0; j < 16; ++j)
                 if (c0 + j < valid) mine[static_cast<size_t>(a * BN + c0 + j) * kBM + m] = __uint_as_float(r[a][j]);
         }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tempty[acc]);
+        released = true;
         // the barrier orders every thread's partial stores before the
-        // leader's fence; the fence (cumulative) then publishes them before
-        // the ticket, and on the reading side orders the ticket before the
-        // partial loads that follow the second barrier
-        ptx::named_bar_sync(1, 128);
-        if (leader) {
-          __threadfence();
-          const int last_now = (atomicAdd(&ph.tickets[w.tile], 1) == ph.split - 1) ? 1 : 0;
-          if (last_now) __threadfence();
-          s_flags[1] = last_now;
-        }
-        ptx::named_bar_sync(1, 128);
-        const int last = *reinterpret_cast<volatile int*>(&s_flags[1]);
+        // leader's release; the leader's acquire and the second barrier order
+        // the ticket before the partial loads of the last arriver
+        ptx::named_bar_sync(bar_id, 128);
+        if (leader) g_flags[1] = (atom_add_acq_rel(&ph.tickets[w.tile], 1) == ph.split - 1) ? 1 : 0;
+        ptx::named_bar_sync(bar_id, 128);
+        const int last = *reinterpret_cast<volatile int*>(&g_flags[1]);
         if (last) {
           const float* tile_parts = ph.partials + static_cast<size_t>(w.tile) * ph.split * slot_elems;
           for (int c0 = 0; c0 < valid; c0 += 16) {
-            uint32_t r[2][16];
-#pragma unroll
-            for (int a = 0; a < C::kNAcc; ++a)
-              if (a < nacc) ptx::tmem_ld16(tb + a * BN + c0, r[a]);
-            ptx::tmem_ld_wait();
             float v[2][16];
 #pragma unroll
             for (int a = 0; a < 2; ++a)
@@ -666,24 +691,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                 const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
 #pragma unroll
                 for (int ss = 0; ss < kMaxSplit; ++ss)
-                  x[a][ss] = (a < nacc && ss < ph.split && ss != w.s)
-                                 ? __ldcg(tile_parts + ss * slot_elems + off) : 0.f;
+                  x[a][ss] = (a < nacc && ss < ph.split) ? __ldcg(tile_parts + ss * slot_elems + off) : 0.f;
               }
 #pragma unroll
               for (int a = 0; a < C::kNAcc; ++a) {
                 if (a >= nacc) continue;
-                float mine_v = 0.f;
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                  if (jj == j) mine_v = __uint_as_float(r[a][jj]);
                 float sum = 0.f;
 #pragma unroll
-                for (int ss = 0; ss < kMaxSplit; ++ss) {
-                  if (ss < ph.split) {
-                    const float xv = (ss == w.s) ? mine_v : x[a][ss];
-                    sum = (ss == 0) ? xv : sum + xv;
-                  }
-                }
+                for (int ss = 0; ss < kMaxSplit; ++ss)
+                  if (ss < ph.split) sum = (ss == 0) ? x[a][ss] : sum + x[a][ss];
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
                   if (jj == j) v[a][jj] = sum;
@@ -694,22 +710,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           if (leader) ph.tickets[w.tile] = 0;
           tile_done = true;
         }
-        ptx::named_bar_sync(1, 128);
+        ptx::named_bar_sync(bar_id, 128);
       }
       if (MODE == 2 && w.phase == 0 && tile_done) {
         // publish this row block of the token tile to the down units waiting on it
-        ptx::named_bar_sync(1, 128);
-        if (leader) {
-          __threadfence();
-          atomicAdd(p.done + w.gtt, 1);
-        }
+        ptx::named_bar_sync(bar_id, 128);
+        if (leader) red_add_release(p.done + w.gtt, 1);
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&tempty[acc]);
-      if (++acc == C::kAccBufs) {
-        acc = 0;
-        acc_phase ^= 1u;
+      if (!released) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tempty[acc]);
       }
+      acc_phase ^= 1u;
     }
   }
 
@@ -834,7 +846,7 @@ int accum_cols(int mode, int bn) { return (mode == 0 ? 2 : 1) * bn; }
 
 }  // namespace
 
-GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms) {
+GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int units_per_sm) {
   GemmPlan plan{};
   const long long entries = static_cast<long long>(T) * K;
   const long long touched = entries < E ? entries : E;
@@ -854,17 +866,18 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms) {
   const long long est = touched * (per_expert > 0 ? per_expert : 1) * n_mb;
   // Units are handed out dynamically, so balance depends on how small the
   // last units are: when tiles are few (decode), split the reduction until
-  // there are at least 16 units per SM, keeping at least 128 KB of weights
-  // per unit (4 k-steps of gate+up rows, 8 of down rows) so that the
-  // per-unit epilogue stays hidden behind the next unit's loads.
+  // there are at least `units_per_sm` units per SM, keeping at least 128 KB
+  // of weights per unit (4 k-steps of gate+up rows, 8 of down rows) so that
+  // the per-unit epilogue stays hidden behind the next unit's loads.
   const int min_ksteps = mode == 0 ? 4 : 8;
   int split = 1;
-  if (est < 16LL * num_sms) {
+  const long long target = static_cast<long long>(units_per_sm) * num_sms;
+  if (est < target) {
     for (int s = 2; s <= ksteps && s <= kMaxSplit; ++s) {
       if (ksteps % s != 0) continue;
       if (ksteps / s < min_ksteps) break;
       split = s;
-      if (est * s >= 16LL * num_sms) break;
+      if (est * s >= target) break;
     }
   }
   plan.split = split;
@@ -970,6 +983,17 @@ cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down,
   prm.max_token_tiles = plan.max_token_tiles;
   return mode == 0 ? launch_mode<0>(plan.bn, prm, num_sms, stream, pdl)
                    : launch_mode<1>(plan.bn, prm, num_sms, stream, pdl);
+}
+
+void plan_experts(int T, int K, int E, int H, int F, int num_sms, GemmPlan* gate_up, GemmPlan* down) {
+  *gate_up = plan_gemm(0, T, K, E, H, F, num_sms);
+  *down = plan_gemm(1, T, K, E, H, F, num_sms);
+  if (fused_experts_supported(*gate_up, *down)) {
+    // One launch runs both phases from one unit list, so only the down units
+    // at its end need to be small for balance; fewer, larger gate/up units
+    // mean fewer split-K tickets, whose round trips the epilogue waits on.
+    *gate_up = plan_gemm(0, T, K, E, H, F, num_sms, 4);
+  }
 }
 
 bool fused_experts_supported(const GemmPlan& gate_up, const GemmPlan& down) {

@@ -63,7 +63,10 @@ struct GemmPlan {
   int max_tiles;        // upper bound on (expert, row-block, token-tile) tiles
 };
 // mode 0: gate/up + SwiGLU (weight rows 2F, reduction H); mode 1: down (rows H, reduction F)
-GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms);
+GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int units_per_sm = 16);
+// The plans of a gate/up + down pass as run by the experts stage (the fused
+// launch when fused_experts_supported, else two launches).
+void plan_experts(int T, int K, int E, int H, int F, int num_sms, GemmPlan* gate_up, GemmPlan* down);
 // Scratch shared by one gate/up + down pass (unit counters, split-K tickets
 // and partial sums); it must be cleared with clear_gemm_scratch before the
 // gate/up GEMM (one memset; each GEMM leaves its tickets at zero).

@@ -48,14 +48,35 @@ __device__ __forceinline__ F2 warp_sum_f2(F2 v) {
   return v;
 }
 
-// 1/sqrt(sum/H + eps) as an fp32 pair, from a double-float sum of squares.
-// GB300 runs fp64 at a small fraction of the fp32 rate, so one thread per
-// token evaluates this and the result is broadcast.
-__device__ __forceinline__ F2 rsqrt_mean(F2 sum, double inv_h, double eps) {
-  const double ms = (static_cast<double>(sum.hi) + static_cast<double>(sum.lo)) * inv_h + eps;
-  const double r = 1.0 / sqrt(ms);
-  const float hi = static_cast<float>(r);
-  return {hi, static_cast<float>(r - static_cast<double>(hi))};
+// 1/sqrt(sum/H + eps) as an fp32 pair, in double-float arithmetic (GB300
+// runs fp64 at a small fraction of the fp32 rate: one fp64 1/sqrt takes about
+// fifteen times as long as this). m = sum * (1/H) + eps is formed as a pair
+// with error-free products; r0 = rsqrtf(m) is within 2^-22 of 1/sqrt(m), and
+// one Newton step carried to second order, r0 (1 + e/2 + 3e^2/8) with
+// e = 1 - m r0^2, leaves a truncation error below 2^-64. The fp32 product
+// a = m_hi r0^2 lies within 2^-21 of 1, so 1 - a is exact and e carries
+// about 2^-46 relative error; so does the pair (2^-48 for a pair rounded from
+// an fp64 1/sqrt).
+__device__ __forceinline__ F2 rsqrt_mean(F2 sum, F2 inv_h, float eps) {
+  const float p = __fmul_rn(sum.hi, inv_h.hi);
+  float pe = fmaf(sum.hi, inv_h.hi, -p);
+  pe = fmaf(sum.hi, inv_h.lo, pe);
+  pe = fmaf(sum.lo, inv_h.hi, pe);
+  const F2 s = two_sum(p, eps);
+  float m_lo = __fadd_rn(s.lo, pe);
+  const float m_hi = __fadd_rn(s.hi, m_lo);
+  m_lo = __fsub_rn(m_lo, __fsub_rn(m_hi, s.hi));
+  const float r0 = rsqrtf(m_hi);
+  const float q = __fmul_rn(r0, r0);
+  const float qe = fmaf(r0, r0, -q);
+  const float a = __fmul_rn(m_hi, q);
+  float ae = fmaf(m_hi, q, -a);
+  ae = fmaf(m_hi, qe, ae);
+  ae = fmaf(m_lo, q, ae);
+  const float e = __fsub_rn(__fsub_rn(1.0f, a), ae);
+  const float corr = __fmul_rn(r0, __fmul_rn(e, fmaf(0.375f, e, 0.5f)));
+  const float hi = __fadd_rn(r0, corr);
+  return {hi, __fsub_rn(corr, __fsub_rn(hi, r0))};
 }
 
 // bf16 bits of the exact value hi + lo, where |lo| <= half an fp32 ulp of hi
@@ -161,9 +182,9 @@ __device__ __forceinline__ uint4 chunk_scale(const uint4& hv, const uint4& wv, c
   return make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16), o[6] | (o[7] << 16));
 }
 
-// block-wide sum of squares -> 1/sqrt(mean + eps), evaluated by thread 0;
+// block-wide sum of squares -> 1/sqrt(mean + eps), evaluated by one thread;
 // red needs 33 entries
-__device__ __forceinline__ F2 block_rsqrt_mean(F2 v, F2* red, int nwarps, double inv_h, double eps) {
+__device__ __forceinline__ F2 block_rsqrt_mean(F2 v, F2* red, int nwarps, F2 inv_h, float eps) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   v = warp_sum_f2(v);
   if (lane == 0) red[w] = v;
@@ -177,6 +198,13 @@ __device__ __forceinline__ F2 block_rsqrt_mean(F2 v, F2* red, int nwarps, double
   const F2 r = red[32];
   __syncthreads();  // red is reused by the next reduction
   return r;
+}
+
+// 1/H as an fp32 pair
+inline F2 inv_hidden(int H) {
+  const double v = 1.0 / H;
+  const float hi = static_cast<float>(v);
+  return {hi, static_cast<float>(v - static_cast<double>(hi))};
 }
 
 // coefficients of the residual add for boundary index n

@@ -13,15 +13,14 @@
 // tokens (redundant but cheap, and it removes a launch and a round trip of
 // z), then dots z with its expert's router row. The last block to finish
 // (ticket counter, zeroed by the host before the launch) writes h' and z, runs
-// the top-k for every token and the permutation of the T*K pairs, copies the
-// permuted rows from the z it holds in registers, and clears the expert
-// GEMMs' counters and tickets. Only that block writes h': h' may alias h, and
-// by then every block has read h.
+// the top-k for every token with the whole block, the permutation of the T*K
+// pairs, copies the permuted rows from the z it holds in registers, and
+// clears the expert GEMMs' counters and tickets. Only that block writes h':
+// h' may alias h, and by then every block has read h.
 #include "common.cuh"
 #include "kernels.h"
 #include "norm_math.cuh"
 #include "ptx.cuh"
-#include "topk.cuh"
 
 namespace beam {
 
@@ -32,6 +31,80 @@ using namespace norm;
 constexpr int kMaxT = 8;
 constexpr int kMaxPairs = 64;
 constexpr int kMaxThreads = 640;  // H <= 5120
+constexpr int kE = 256;           // experts (8 groups of 32)
+constexpr int kMaxK = 16;
+
+// Shared memory of the block top-k: up to two tokens at once (256 threads each)
+struct TopkSmem {
+  float sb[2][kE];       // biased scores
+  float gs[2][8];        // group scores
+  float slot_s[2][kMaxK];
+  int slot_id[2][kMaxK];
+};
+
+// Group-limited top-k of token t over 256 experts in 8 groups of 32, one
+// thread per expert (q) and one warp per group, by ranks: a candidate in the
+// TG chosen groups takes slot r = the number of chosen candidates that beat
+// it (higher biased score, ties to the lower index), which is the order K
+// rounds of argmax would pick. Same values as the warp version (topk.cuh):
+// the same sigmoid, group scores as the sum of the group's two largest biased
+// scores (with multiplicity), weights normalised in slot order.
+__device__ __forceinline__ void topk_block_phase1(const float* logits, float bias_q, int t, int q, int gi,
+                                                  TopkSmem& sm, float& s_out) {
+  const int lane = q & 31;
+  const float l = __ldcg(logits + static_cast<size_t>(t) * kE + q);
+  const float s = 1.0f / (1.0f + expf(-l));
+  const float sb = s + bias_q;
+  sm.sb[gi][q] = sb;
+  float top1 = sb;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) top1 = fmaxf(top1, __shfl_xor_sync(kFullMask, top1, o));
+  const unsigned eq = __ballot_sync(kFullMask, sb == top1);
+  float v = (eq != 0u && lane == __ffs(eq) - 1) ? -INFINITY : sb;  // drop one instance of the maximum
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+  if (lane == 0) sm.gs[gi][q >> 5] = top1 + v;
+  if (q < kMaxK) {  // a slot no candidate takes (non-finite scores) reads as a dropped pair
+    sm.slot_id[gi][q] = -1;
+    sm.slot_s[gi][q] = 0.f;
+  }
+  s_out = s;
+}
+
+__device__ __forceinline__ void topk_block_phase2(int q, int gi, int TG, int K, float s, TopkSmem& sm) {
+  unsigned chosen = 0;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float gv = sm.gs[gi][g];
+    int rank = 0;
+#pragma unroll
+    for (int o = 0; o < 8; ++o) {
+      const float ov = sm.gs[gi][o];
+      rank += (ov > gv) || (ov == gv && o < g);
+    }
+    if (rank < TG) chosen |= 1u << g;
+  }
+  if (!((chosen >> (q >> 5)) & 1u)) return;
+  const float sb = sm.sb[gi][q];
+  int rank = 0;
+  for (int g = 0; g < 8; ++g) {
+    if (!((chosen >> g) & 1u)) continue;
+    const float4* row = reinterpret_cast<const float4*>(&sm.sb[gi][g * 32]);
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+      const float4 o = row[j4];
+      const int j = g * 32 + j4 * 4;
+      rank += (o.x > sb) || (o.x == sb && j < q);
+      rank += (o.y > sb) || (o.y == sb && j + 1 < q);
+      rank += (o.z > sb) || (o.z == sb && j + 2 < q);
+      rank += (o.w > sb) || (o.w == sb && j + 3 < q);
+    }
+  }
+  if (rank < K) {
+    sm.slot_id[gi][rank] = q;
+    sm.slot_s[gi][rank] = s;
+  }
+}
 
 // TMAX: token capacity of the register arrays. Up to two tokens, two blocks
 // fit on an SM, so all 256 expert blocks are resident at once on 152 SMs.
@@ -39,7 +112,7 @@ template <int TMAX>
 __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
     route_decode_kernel(const uint4* h, const uint4* __restrict__ x, const uint4* __restrict__ w_post,
                         const uint4* __restrict__ w_pre, const float* __restrict__ W, const float* __restrict__ bias,
-                        int T, int E, int G, int TG, int K, float scale, double inv_h, double eps, ResidualCoef coef,
+                        int T, int E, int G, int TG, int K, float scale, F2 inv_h, float eps, ResidualCoef coef,
                         uint4* h_out, uint4* __restrict__ z_out, float* __restrict__ logits,
                         int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_perm, uint4* __restrict__ x_perm,
@@ -49,6 +122,7 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
   __shared__ int hist[256];
   __shared__ int s_pos[kMaxPairs];
   __shared__ int s_ids[kMaxPairs];
+  __shared__ __align__(16) TopkSmem tk;
   __shared__ int s_last;
   const int c = threadIdx.x;  // 8-element chunk owned by this thread
   const int nc = blockDim.x;
@@ -61,6 +135,7 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
   const float4 wa = __ldg(wrow + 2 * c), wb = __ldg(wrow + 2 * c + 1);
   const uint4 wp = w_post[c];
   const uint4 wq = w_pre[c];
+  const float bias_q = c < 2 * kE ? __ldg(bias + c % kE) : 0.f;  // the top-k's expert c % 256
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
@@ -120,9 +195,27 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
     }
   }
 
-  for (int t = warp; t < T; t += nwarps)
-    topk_lanes_token<8, 4>(logits, bias, t, G, TG, K, scale, ids, wout, s_ids + t * K);
-  __syncthreads();
+  // top-k, up to two tokens at once (256 threads each)
+  const int ngrp = nc >= 2 * kE ? 2 : 1;
+  const int gi = c / kE, q = c % kE;
+  for (int t0 = 0; t0 < T; t0 += ngrp) {
+    const int t = t0 + gi;
+    const bool act = gi < ngrp && t < T;
+    float s = 0.f;
+    if (act) topk_block_phase1(logits, bias_q, t, q, gi, tk, s);
+    __syncthreads();
+    if (act) topk_block_phase2(q, gi, TG, K, s, tk);
+    __syncthreads();
+    if (act && q < K) {
+      float total = 0.f;
+      for (int k = 0; k < K; ++k) total += tk.slot_s[gi][k];
+      const int id = tk.slot_id[gi][q];
+      ids[static_cast<size_t>(t) * K + q] = id;
+      wout[static_cast<size_t>(t) * K + q] = scale * tk.slot_s[gi][q] / total;
+      s_ids[t * K + q] = id;
+    }
+    __syncthreads();
+  }
 
   const int pairs = T * K;
   if (warp == 0) {
@@ -196,8 +289,8 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
 }  // namespace
 
 bool route_decode_supported(int T, int H, int E, int G, int K) {
-  return T >= 1 && T <= kMaxT && E == 256 && G == 8 && T * K <= kMaxPairs && H % 256 == 0 &&
-         H / 8 <= kMaxThreads;
+  return T >= 1 && T <= kMaxT && E == kE && G == 8 && K <= kMaxK && T * K <= kMaxPairs && H % 256 == 0 &&
+         H / 8 >= kE && H / 8 <= kMaxThreads;
 }
 
 cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
@@ -209,12 +302,12 @@ cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint
   cudaError_t err = cudaMemsetAsync(ticket, 0, sizeof(int), stream);
   if (err != cudaSuccess) return err;
   const ResidualCoef coef = norm::residual_coef(n);
+  const F2 inv_h = norm::inv_hidden(H);
   auto kernel = T <= 1 ? route_decode_kernel<1> : T <= 2 ? route_decode_kernel<2>
               : T <= 4 ? route_decode_kernel<4> : route_decode_kernel<8>;
   err = launch_kernel(kernel, dim3(E), dim3(H / 8), 0, stream, pdl, reinterpret_cast<const uint4*>(h),
                       reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(w_post),
-                      reinterpret_cast<const uint4*>(w_pre), W, bias, T, E, G, TG, K, scale, 1.0 / H,
-                      static_cast<double>(eps), coef, reinterpret_cast<uint4*>(h_out), reinterpret_cast<uint4*>(z_out),
+                      reinterpret_cast<const uint4*>(w_pre), W, bias, T, E, G, TG, K, scale, inv_h, eps, coef, reinterpret_cast<uint4*>(h_out), reinterpret_cast<uint4*>(z_out),
                       logits, ids, w, offsets, perm_token, inv_perm, reinterpret_cast<uint4*>(x_perm), ticket,
                       static_cast<int*>(clear), static_cast<int>(clear_bytes / sizeof(int)));
   ++launch_counter();

@@ -1,6 +1,5 @@
 // Group-limited top-k for one token in one warp, for layouts where every
-// group covers whole lanes; shared by the router kernels and the fused decode
-// routing kernel.
+// group covers whole lanes (the router kernels).
 #pragma once
 
 #include "common.cuh"
@@ -14,11 +13,10 @@ namespace beam {
 // group's lanes; the TG groups are chosen by rank; the K experts by K rounds
 // of a warp argmax (ties to the lower index), which also yields the slot
 // order. The weights sum in slot order exactly as the generic kernel does.
-// `s_ids` (optional) receives a copy of the token's K ids, e.g. in shared memory.
 template <int EPL, int LPG>
 __device__ __forceinline__ void topk_lanes_token(const float* logits, const float* __restrict__ bias, int t, int G,
                                                  int TG, int K, float scale, int32_t* __restrict__ ids,
-                                                 float* __restrict__ wout, int32_t* s_ids = nullptr) {
+                                                 float* __restrict__ wout) {
   const int lane = threadIdx.x & 31;
   constexpr int E = 32 * EPL;
   float s[EPL], sb[EPL];
@@ -99,7 +97,6 @@ __device__ __forceinline__ void topk_lanes_token(const float* logits, const floa
     }
   }
   if (lane < K) {
-    if (s_ids != nullptr) s_ids[lane] = id_sel;
     ids[static_cast<size_t>(t) * K + lane] = id_sel;
     wout[static_cast<size_t>(t) * K + lane] = scale * s_sel / total;
   }
