@@ -118,7 +118,7 @@ LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
   l.perm = o;         o = align_up(o + rows * 4);
   l.inv = o;          o = align_up(o + rows * 4);
   l.perm_scratch = o; o = align_up(o + beam::permute_scratch_bytes(T, c->topk, c->num_experts));
-  l.router_ticket = o; o = align_up(o + sizeof(int));
+  l.router_ticket = o; o = align_up(o + beam::kRouteSyncInts * sizeof(int));
   l.x_perm = o;       o = align_up(o + rows * c->hidden * 2);
   l.experts = o;      o = align_up(o + experts_ws(c, T, sms).total);
   l.total = o;
@@ -141,7 +141,7 @@ void record(const beam_moe_debug_t* dbg, int i, cudaStream_t s) {
 beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gu, const uint16_t* w_d,
                           const float* topk_w, const int32_t* inv, int T, const beam_moe_config_t* c, uint16_t* y,
                           char* ws, int sms, cudaStream_t s, const beam_moe_debug_t* dbg = nullptr, bool pdl = false,
-                          bool cleared = false) {
+                          bool cleared = false, const int* ready = nullptr) {
   const ExpertsWs w = experts_ws(c, T, sms);
   const int rows = T * c->topk;
   uint16_t* act = reinterpret_cast<uint16_t*>(ws + w.act);
@@ -156,7 +156,7 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
   if (beam::fused_experts_supported(p0, p1)) {
     // both GEMMs in one launch (the per-stage events bracket it as gate/up; down reads 0)
     e = beam::launch_fused_experts(p0, p1, w_gu, w_d, x_perm, offsets, rows, c->num_experts, c->hidden, c->d_ff,
-                                   act, y_perm, g, sms, s, pdl);
+                                   act, y_perm, g, sms, s, pdl, ready);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
     record(dbg, 4, s);
   } else {
@@ -405,18 +405,20 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
   cudaError_t e;
   if (beam::route_decode_supported(T, H, cfg->num_experts, cfg->num_groups, cfg->topk)) {
     // decode sizes: boundary, router, top-k, permutation and the GEMM scratch
-    // clear in one launch (the stage events of router and permutation are empty)
+    // clear in one launch (the stage events of router and permutation are
+    // empty); the fused experts launch starts on the routing kernel's flags
     e = beam::launch_route_decode(h, x, wt->w_post, wt->w_pre, wt->router_w, wt->bias, T, H, cfg->num_experts,
                                   cfg->num_groups, cfg->topk_groups, cfg->topk, cfg->routed_scale, cfg->eps, n,
                                   h_out, z, logits, ids, w, offsets, perm, inv, x_perm, router_ticket, gemm_scratch,
-                                  beam::gemm_clear_bytes(p0, p1), s, pdl);
+                                  beam::gemm_clear_bytes(p0, p1), d.sms, s, pdl);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
     record(dbg, 1, s);
     record(dbg, 2, s);
     launches += launch_counter();
     launch_counter() = 0;
+    const int* ready = beam::fused_experts_supported(p0, p1) ? router_ticket + 1 : nullptr;
     st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
-                     dbg, pdl, /*cleared=*/true);
+                     dbg, pdl, /*cleared=*/true, ready);
     launch_counter() += launches;
     return st;
   }

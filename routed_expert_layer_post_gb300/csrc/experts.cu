@@ -87,6 +87,10 @@ struct GemmParams {
   int E;
   int rows;              // permuted rows (T * K)
   int max_token_tiles;   // MODE 2: size of `done`
+  // MODE 2 (optional): flags of the routing kernel before this launch; [0]
+  // set once offsets and scratch are valid, [1] once the activation rows are
+  // (polled instead of waiting for that kernel to end)
+  const int* ready;
 };
 
 constexpr int pow2_at_least(int v) {
@@ -290,7 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   // streams weight tiles now; only its activation loads and its epilogue wait
   // for the gate/up GEMM.
   if (MODE != 1) {
-    ptx::griddep_wait();
+    if (MODE == 2 && p.ready != nullptr) {
+      if (tid == 0 && !wait_counter(p.ready, 1, abort_flag, 9)) s_flags[2] = 1;
+      __syncthreads();  // thread 0's acquire orders the offset and counter reads below
+    } else {
+      ptx::griddep_wait();
+    }
     ptx::griddep_launch_dependents();
   }
   for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
@@ -334,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     if (tid == 0) atomicCAS(&g_device_error, 0, 100);
     n_tiles0 = 0;  // workspace too small for this routing: do nothing rather than overrun it
   }
+  if (MODE == 2 && s_flags[2]) n_tiles0 = 0;  // the routing flags never came: do nothing
   const int n_units0 = n_tiles0 * p.ph[0].split;
   int n_units = n_units0;
   if (MODE == 2 && n_tiles0 > 0) {
@@ -355,14 +365,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      // MODE 1: activation (B) loads wait for the previous kernel; until then
-      // stages get their weight tile only and are remembered here
-      bool dep_ready = (MODE != 1);
+      // MODE 1: activation (B) loads wait for the previous kernel; MODE 2 with
+      // routing flags: they wait for the flag of the permuted rows. Until then
+      // stages get their weight tile only and are remembered here.
+      bool dep_ready = (MODE == 0) || (MODE == 2 && p.ready == nullptr);
       int npend = 0;
       int pend_stage[C::kStages], pend_k[C::kStages], pend_row[C::kStages];
       auto release_pending = [&]() {
-        ptx::griddep_wait();
-        ptx::griddep_launch_dependents();
+        if (MODE == 1) {
+          ptx::griddep_wait();
+          ptx::griddep_launch_dependents();
+        } else {
+          if (!wait_counter(p.ready + 1, 1, abort_flag, 10)) ok = false;
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
+        }
         for (int i = 0; i < npend; ++i)
           ptx::tma_load_2d(tiles + pend_stage[i] * C::kStageBytes + C::kNAcc * kTileABytes, &p.ph[0].tmap_x,
                            &full[pend_stage[i]], pend_k[i] * kBK, pend_row[i], pol_x);
@@ -427,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const int k0 = w.s * ph.ksteps / ph.split, k1 = (w.s + 1) * ph.ksteps / ph.split;
         const int row0 = s_off[w.e] + w.tt * BN;
         bool defer = false;
+        if (MODE == 2 && w.phase == 1 && !dep_ready) release_pending();  // pending rows first: one list at a time
         if (MODE == 2 && w.phase == 1) {
           // this token tile's rows of `act` come from gate/up units held by
           // running CTAs (all gate/up units are handed out before any down
@@ -683,26 +700,36 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[a][j] = 0.f;
             for (int j = 0; j < 16 && c0 + j < valid; ++j) {
-              // all partials of this column are requested before any is added,
-              // then summed in split order (the result does not depend on timing)
-              float x[C::kNAcc][kMaxSplit];
+              // partials are requested eight splits at a time and summed in
+              // split order (the result does not depend on timing). The loop
+              // stays rolled: this path runs once per tile, and its first run
+              // on an SM fetches its instructions while HBM is saturated.
+              float sum[C::kNAcc];
 #pragma unroll
-              for (int a = 0; a < C::kNAcc; ++a) {
-                const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
+              for (int a = 0; a < C::kNAcc; ++a) sum[a] = 0.f;
+#pragma unroll 1
+              for (int s0 = 0; s0 < ph.split; s0 += 8) {
+                float x[C::kNAcc][8];
 #pragma unroll
-                for (int ss = 0; ss < kMaxSplit; ++ss)
-                  x[a][ss] = (a < nacc && ss < ph.split) ? __ldcg(tile_parts + ss * slot_elems + off) : 0.f;
+                for (int a = 0; a < C::kNAcc; ++a) {
+                  const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
+#pragma unroll
+                  for (int i = 0; i < 8; ++i)
+                    x[a][i] = (a < nacc && s0 + i < ph.split) ? __ldcg(tile_parts + (s0 + i) * slot_elems + off)
+                                                               : 0.f;
+                }
+#pragma unroll
+                for (int a = 0; a < C::kNAcc; ++a)
+#pragma unroll
+                  for (int i = 0; i < 8; ++i)
+                    if (s0 + i < ph.split) sum[a] = (s0 + i == 0) ? x[a][i] : sum[a] + x[a][i];
               }
 #pragma unroll
               for (int a = 0; a < C::kNAcc; ++a) {
                 if (a >= nacc) continue;
-                float sum = 0.f;
-#pragma unroll
-                for (int ss = 0; ss < kMaxSplit; ++ss)
-                  if (ss < ph.split) sum = (ss == 0) ? x[a][ss] : sum + x[a][ss];
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
-                  if (jj == j) v[a][jj] = sum;
+                  if (jj == j) v[a][jj] = sum[a];
               }
             }
             store_outputs<BN>(ph, p.rows, kind, v, c0, valid, row0, col);
@@ -731,6 +758,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  // with routing flags the routing kernel may still be running: end after it,
+  // so that kernels waiting on this one also see everything it wrote
+  if (MODE == 2 && p.ready != nullptr) ptx::griddep_wait();
 }
 
 // ------------------------------------------------------------------ combine
@@ -1003,7 +1033,7 @@ bool fused_experts_supported(const GemmPlan& gate_up, const GemmPlan& down) {
 cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* w_gate_up,
                                  const uint16_t* w_down, const uint16_t* x_perm, const int32_t* offsets, int rows,
                                  int E, int H, int F, uint16_t* act, uint16_t* y_perm, void* scratch, int num_sms,
-                                 cudaStream_t stream, bool pdl) {
+                                 cudaStream_t stream, bool pdl, const int* ready) {
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
   char* base = static_cast<char*>(scratch);
@@ -1017,6 +1047,7 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
   prm.E = E;
   prm.rows = rows;
   prm.max_token_tiles = gate_up.max_token_tiles;
+  prm.ready = ready;
   switch (gate_up.bn) {
     case 16: return launch_fused_bn<16>(prm, num_sms, stream, pdl);
     case 32: return launch_fused_bn<32>(prm, num_sms, stream, pdl);

@@ -37,15 +37,18 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 // ---- decode routing (route_decode.cu)
 // Boundary -> router -> top-k -> permutation -> row gather in one launch, and
 // `clear_bytes` of `clear` zeroed (the experts' counters and tickets), for
-// T <= 8 with 256 experts in 8 groups. `ticket` is zeroed by a memset before
-// the launch and left zero.
+// T <= 8 with 256 experts in 8 groups. `sync` (kRouteSyncInts ints, zeroed by
+// a memset before the launch): [0] the blocks' ticket (left zero), [1] set
+// once offsets, permutation and the cleared scratch are valid, [2] set once
+// the permuted rows are valid (the fused experts launch polls [1] and [2]).
+constexpr int kRouteSyncInts = 4;
 bool route_decode_supported(int T, int H, int E, int G, int K);
 cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
                                 const float* W, const float* bias, int T, int H, int E, int G, int TG, int K,
                                 float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
                                 int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
-                                uint16_t* x_perm, int* ticket, void* clear, size_t clear_bytes, cudaStream_t stream,
-                                bool pdl);
+                                uint16_t* x_perm, int* sync, void* clear, size_t clear_bytes, int num_sms,
+                                cudaStream_t stream, bool pdl);
 
 // ---- permutation (permute.cu)
 size_t permute_scratch_bytes(int T, int K, int E);
@@ -76,10 +79,13 @@ size_t gemm_clear_bytes(const GemmPlan& gate_up, const GemmPlan& down);
 // Both GEMMs in one persistent launch (down units of a token tile wait for the
 // gate/up tiles that produce its rows); needs equal token tiles of <= 64.
 bool fused_experts_supported(const GemmPlan& gate_up, const GemmPlan& down);
+// `ready` (optional): the decode routing kernel's flags [1] and [2]; the launch
+// then reads offsets and scratch once [1] is set and the permuted rows once
+// [2] is set, instead of waiting for the previous kernel to finish.
 cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* w_gate_up,
                                  const uint16_t* w_down, const uint16_t* x_perm, const int32_t* offsets, int rows,
                                  int E, int H, int F, uint16_t* act, uint16_t* y_perm, void* scratch, int num_sms,
-                                 cudaStream_t stream, bool pdl);
+                                 cudaStream_t stream, bool pdl, const int* ready = nullptr);
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl = false);

@@ -8,15 +8,19 @@
 // top-2-sum group scores, TG groups, K experts, weights * routed_scale, and
 // the stable (expert, token) order.
 //
-// One block per expert, one thread per 8 hidden elements. At decode the
-// token rows are ~10 KB, so every block recomputes the boundary for the
-// tokens (redundant but cheap, and it removes a launch and a round trip of
-// z), then dots z with its expert's router row. The last block to finish
-// (ticket counter, zeroed by the host before the launch) writes h' and z, runs
-// the top-k for every token with the whole block, the permutation of the T*K
-// pairs, copies the permuted rows from the z it holds in registers, and
-// clears the expert GEMMs' counters and tickets. Only that block writes h':
-// h' may alias h, and by then every block has read h.
+// One block per SM (one or two experts each), one thread per 8 hidden
+// elements. At decode the token rows are ~10 KB, so every block recomputes the
+// boundary for the tokens (it removes a launch and a round trip of z; one
+// block per SM keeps the redundant arithmetic at one copy per SM), then dots z
+// with its experts' router rows. The last block to finish (ticket counter)
+// writes h' and z, runs the top-k for every token with the whole block and the
+// permutation of the T*K pairs, clears the expert GEMMs' counters and
+// tickets, raises the first ready flag (offsets and scratch valid), copies the
+// permuted rows from the z it holds in registers and raises the second (rows
+// valid). The experts launch that follows polls those flags instead of waiting
+// for this kernel to end. Only the last block writes h': h' may alias h, and
+// by then every block has read h. Ticket and flags are zeroed by the host
+// before the launch; the ticket is left zero.
 #include "common.cuh"
 #include "kernels.h"
 #include "norm_math.cuh"
@@ -33,6 +37,10 @@ constexpr int kMaxPairs = 64;
 constexpr int kMaxThreads = 640;  // H <= 5120
 constexpr int kE = 256;           // experts (8 groups of 32)
 constexpr int kMaxK = 16;
+
+__device__ __forceinline__ void red_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // Shared memory of the block top-k: up to two tokens at once (256 threads each)
 struct TopkSmem {
@@ -106,19 +114,18 @@ __device__ __forceinline__ void topk_block_phase2(int q, int gi, int TG, int K, 
   }
 }
 
-// TMAX: token capacity of the register arrays. Up to two tokens, two blocks
-// fit on an SM, so all 256 expert blocks are resident at once on 152 SMs.
+// TMAX: token capacity of the register arrays
 template <int TMAX>
-__global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
+__global__ void __launch_bounds__(kMaxThreads, 1)
     route_decode_kernel(const uint4* h, const uint4* __restrict__ x, const uint4* __restrict__ w_post,
                         const uint4* __restrict__ w_pre, const float* __restrict__ W, const float* __restrict__ bias,
                         int T, int E, int G, int TG, int K, float scale, F2 inv_h, float eps, ResidualCoef coef,
                         uint4* h_out, uint4* __restrict__ z_out, float* __restrict__ logits,
                         int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_perm, uint4* __restrict__ x_perm,
-                        int* ticket, int* __restrict__ clear, int clear_ints) {
+                        int* sync, int* __restrict__ clear, int clear_ints) {
   __shared__ F2 red[33];
-  __shared__ float fred[32];
+  __shared__ float fred[32], fred2[32];
   __shared__ int hist[256];
   __shared__ int s_pos[kMaxPairs];
   __shared__ int s_ids[kMaxPairs];
@@ -128,11 +135,15 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
   const int nc = blockDim.x;
   const int nwarps = nc >> 5;
   const int lane = c & 31, warp = c >> 5;
-  const int e = blockIdx.x;
+  // experts of this block: e0 and e1 (e1 < E for the first E - gridDim.x blocks)
+  const int e0 = blockIdx.x, e1 = blockIdx.x + gridDim.x;
+  const bool two = e1 < E;
 
   // constants first: they do not depend on the previous kernel
-  const float4* wrow = reinterpret_cast<const float4*>(W + static_cast<size_t>(e) * nc * 8);
-  const float4 wa = __ldg(wrow + 2 * c), wb = __ldg(wrow + 2 * c + 1);
+  const float4* wrow0 = reinterpret_cast<const float4*>(W + static_cast<size_t>(e0) * nc * 8);
+  const float4* wrow1 = reinterpret_cast<const float4*>(W + static_cast<size_t>(two ? e1 : e0) * nc * 8);
+  const float4 wa0 = __ldg(wrow0 + 2 * c), wb0 = __ldg(wrow0 + 2 * c + 1);
+  const float4 wa1 = __ldg(wrow1 + 2 * c), wb1 = __ldg(wrow1 + 2 * c + 1);
   const uint4 wp = w_post[c];
   const uint4 wq = w_pre[c];
   const float bias_q = c < 2 * kE ? __ldg(bias + c % kE) : 0.f;  // the top-k's expert c % 256
@@ -155,24 +166,40 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
       hc[t] = chunk_residual(xv, hv, wp, r, coef, acc2);
       const F2 r2 = block_rsqrt_mean(acc2, red, nwarps, inv_h, eps);
       zc[t] = chunk_scale(hc[t], wq, r2);
-      // router logit of expert e: z . W_r[e] in fp32 FMA, fixed reduction order
+      // router logits of the block's experts: z . W_r[e] in fp32 FMA, fixed reduction order
       float zf[8];
       unpack8(zc[t], zf);
-      float dot = 0.f;
-      dot = fmaf(zf[0], wa.x, dot);
-      dot = fmaf(zf[1], wa.y, dot);
-      dot = fmaf(zf[2], wa.z, dot);
-      dot = fmaf(zf[3], wa.w, dot);
-      dot = fmaf(zf[4], wb.x, dot);
-      dot = fmaf(zf[5], wb.y, dot);
-      dot = fmaf(zf[6], wb.z, dot);
-      dot = fmaf(zf[7], wb.w, dot);
-      dot = warp_sum(dot);
-      if (lane == 0) fred[warp] = dot;
+      float d0 = 0.f, d1 = 0.f;
+      d0 = fmaf(zf[0], wa0.x, d0);
+      d0 = fmaf(zf[1], wa0.y, d0);
+      d0 = fmaf(zf[2], wa0.z, d0);
+      d0 = fmaf(zf[3], wa0.w, d0);
+      d0 = fmaf(zf[4], wb0.x, d0);
+      d0 = fmaf(zf[5], wb0.y, d0);
+      d0 = fmaf(zf[6], wb0.z, d0);
+      d0 = fmaf(zf[7], wb0.w, d0);
+      d1 = fmaf(zf[0], wa1.x, d1);
+      d1 = fmaf(zf[1], wa1.y, d1);
+      d1 = fmaf(zf[2], wa1.z, d1);
+      d1 = fmaf(zf[3], wa1.w, d1);
+      d1 = fmaf(zf[4], wb1.x, d1);
+      d1 = fmaf(zf[5], wb1.y, d1);
+      d1 = fmaf(zf[6], wb1.z, d1);
+      d1 = fmaf(zf[7], wb1.w, d1);
+      d0 = warp_sum(d0);
+      d1 = warp_sum(d1);
+      if (lane == 0) {
+        fred[warp] = d0;
+        fred2[warp] = d1;
+      }
       __syncthreads();
       if (warp == 0) {
-        const float s = warp_sum(lane < nwarps ? fred[lane] : 0.f);
-        if (lane == 0) logits[static_cast<size_t>(t) * E + e] = s;
+        const float s0 = warp_sum(lane < nwarps ? fred[lane] : 0.f);
+        const float s1 = warp_sum(lane < nwarps ? fred2[lane] : 0.f);
+        if (lane == 0) {
+          logits[static_cast<size_t>(t) * E + e0] = s0;
+          if (two) logits[static_cast<size_t>(t) * E + e1] = s1;
+        }
       }
       __syncthreads();
     }
@@ -181,7 +208,8 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
   // the last block to finish sees every expert's logits
   __threadfence();
   __syncthreads();
-  if (c == 0) s_last = (atomicAdd(ticket, 1) == E - 1);
+  int* ticket = sync;
+  if (c == 0) s_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -271,7 +299,11 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
       }
     }
   }
+  for (int j = c; j < clear_ints; j += nc) clear[j] = 0;
+  // offsets, permutation and cleared scratch are published together (the
+  // barrier orders every thread's stores before thread 0's release)
   __syncthreads();
+  if (c == 0) red_release(sync + 1, 1);
   // permuted rows straight from the z this block holds
   for (int i = 0; i < pairs; ++i) {
     if (s_pos[i] < 0) continue;
@@ -282,11 +314,18 @@ __global__ void __launch_bounds__(kMaxThreads, TMAX <= 2 ? 2 : 1)
       if (tt == t) v = zc[tt];
     x_perm[static_cast<size_t>(s_pos[i]) * nc + c] = v;
   }
-  for (int j = c; j < clear_ints; j += nc) clear[j] = 0;
-  if (c == 0) *ticket = 0;
+  __syncthreads();
+  if (c == 0) {
+    red_release(sync + 2, 1);
+    *ticket = 0;
+  }
 }
 
 }  // namespace
+
+int route_decode_blocks(int E, int num_sms) {
+  return num_sms < E / 2 ? E / 2 : (num_sms > E ? E : num_sms);
+}
 
 bool route_decode_supported(int T, int H, int E, int G, int K) {
   return T >= 1 && T <= kMaxT && E == kE && G == 8 && K <= kMaxK && T * K <= kMaxPairs && H % 256 == 0 &&
@@ -297,18 +336,19 @@ cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint
                                 const float* W, const float* bias, int T, int H, int E, int G, int TG, int K,
                                 float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
                                 int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
-                                uint16_t* x_perm, int* ticket, void* clear, size_t clear_bytes, cudaStream_t stream,
-                                bool pdl) {
-  cudaError_t err = cudaMemsetAsync(ticket, 0, sizeof(int), stream);
+                                uint16_t* x_perm, int* sync, void* clear, size_t clear_bytes, int num_sms,
+                                cudaStream_t stream, bool pdl) {
+  cudaError_t err = cudaMemsetAsync(sync, 0, kRouteSyncInts * sizeof(int), stream);
   if (err != cudaSuccess) return err;
   const ResidualCoef coef = norm::residual_coef(n);
   const F2 inv_h = norm::inv_hidden(H);
   auto kernel = T <= 1 ? route_decode_kernel<1> : T <= 2 ? route_decode_kernel<2>
               : T <= 4 ? route_decode_kernel<4> : route_decode_kernel<8>;
-  err = launch_kernel(kernel, dim3(E), dim3(H / 8), 0, stream, pdl, reinterpret_cast<const uint4*>(h),
+  err = launch_kernel(kernel, dim3(route_decode_blocks(E, num_sms)), dim3(H / 8), 0, stream, pdl,
+                      reinterpret_cast<const uint4*>(h),
                       reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(w_post),
                       reinterpret_cast<const uint4*>(w_pre), W, bias, T, E, G, TG, K, scale, inv_h, eps, coef, reinterpret_cast<uint4*>(h_out), reinterpret_cast<uint4*>(z_out),
-                      logits, ids, w, offsets, perm_token, inv_perm, reinterpret_cast<uint4*>(x_perm), ticket,
+                      logits, ids, w, offsets, perm_token, inv_perm, reinterpret_cast<uint4*>(x_perm), sync,
                       static_cast<int*>(clear), static_cast<int>(clear_bytes / sizeof(int)));
   ++launch_counter();
   return err;
