@@ -103,7 +103,7 @@ ExpertsWs experts_ws(const beam_moe_config_t* c, int T, int sms) {
 }
 
 struct LayerWs {
-  size_t z, logits, ids, w, offsets, perm, inv, perm_scratch, router_ticket, x_perm, experts, total;
+  size_t z, logits, ids, w, offsets, perm, inv, perm_scratch, router_ticket, router_w3, x_perm, experts, total;
 };
 
 LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
@@ -119,6 +119,9 @@ LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
   l.inv = o;          o = align_up(o + rows * 4);
   l.perm_scratch = o; o = align_up(o + beam::permute_scratch_bytes(T, c->topk, c->num_experts));
   l.router_ticket = o; o = align_up(o + beam::kRouteSyncInts * sizeof(int));
+  l.router_w3 = o;
+  if (beam::router_tc_supported(T, c->num_experts, c->hidden))
+    o = align_up(o + beam::router_tc_scratch_bytes(c->num_experts, c->hidden));
   l.x_perm = o;       o = align_up(o + rows * c->hidden * 2);
   l.experts = o;      o = align_up(o + experts_ws(c, T, sms).total);
   l.total = o;
@@ -434,7 +437,11 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
                                        router_ticket, s, pdl);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   } else {
-    e = beam::launch_router_logits(z, wt->router_w, T, H, cfg->num_experts, logits, s, pdl);
+    if (beam::router_tc_supported(T, cfg->num_experts, H))
+      e = beam::launch_router_tc(z, wt->router_w, T, cfg->num_experts, H, logits,
+                                 reinterpret_cast<uint16_t*>(base + L.router_w3), d.sms, s, pdl);
+    else
+      e = beam::launch_router_logits(z, wt->router_w, T, H, cfg->num_experts, logits, s, pdl);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
     e = beam::launch_topk(logits, wt->bias, T, cfg->num_experts, cfg->num_groups, cfg->topk_groups, cfg->topk,
                           cfg->routed_scale, ids, w, s, pdl);

@@ -805,6 +805,166 @@ __global__ void __launch_bounds__(256)
   y[idx] = pack8(acc);
 }
 
+// ------------------------------------------------------------------ tensor-core FP32 router
+// logits[t][e] = sum_k z[t][k] * W[e][k] for prefill sizes. Each fp32 weight
+// is split exactly into three bf16 terms, W = hi + mid + lo (hi = bf16(W),
+// mid = bf16(W - hi), lo = W - hi - mid, which fits bf16 because W has 24
+// significand bits). z is bf16, so every product is exact in fp32. The tensor
+// core adds them in fp32 but does not round each addition like an IEEE adder,
+// and over the whole reduction that measured 2.3e-5 of the row's largest
+// logit, above the router's 1e-5 bar. So each 64-wide k-step (its three terms,
+// 192 products) accumulates in a fresh TMEM buffer, and the epilogue adds the
+// 80 k-step sums in fp32 registers in k order.
+__global__ void __launch_bounds__(256)
+    split_router_weights_kernel(const float* __restrict__ W, uint16_t* __restrict__ w3, size_t n) {
+  ptx::griddep_wait();  // w3 may still be read by an earlier router launch
+  ptx::griddep_launch_dependents();
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float w = W[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = __fsub_rn(w, __bfloat162float(hi));  // exact
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = __fsub_rn(r1, __bfloat162float(mid));  // exact, at most 8 significant bits
+    w3[i] = __bfloat16_as_ushort(hi);
+    w3[n + i] = __bfloat16_as_ushort(mid);
+    w3[2 * n + i] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+  }
+}
+
+constexpr int kRtStages = 3;
+constexpr int kRtThreads = 192;
+
+// One CTA per (128 experts, BN tokens) tile. Warp 0 issues TMA: the three
+// weight terms of a 64-wide k-step as one 3-D box, and the token tile. Warp 1
+// issues 12 MMAs per k-step into one accumulator. Warps 2-5 read TMEM (lane =
+// expert, column = token) and store fp32 logits.
+template <int BN>
+__global__ void __launch_bounds__(kRtThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tmap_w3, const __grid_constant__ CUtensorMap tmap_z, int T,
+                     int E, int ksteps, float* __restrict__ logits) {
+  constexpr uint32_t kA = 3 * kTileABytes;
+  constexpr uint32_t kStage = kA + BN * kBK * 2;
+  static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t full[kRtStages], empty[kRtStages], tfull[2], tempty[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM;
+  constexpr uint32_t kCols = 2 * BN;  // two k-step buffers
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRtStages; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&tfull[i], 1);
+      ptx::mbar_init(&tempty[i], 128);
+    }
+    abort_s = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmap_w3);
+    ptx::prefetch_tensormap(&tmap_z);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&tmem_slot, kCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_flag = &abort_s;
+  ptx::griddep_wait();  // z and the split weights come from the previous kernels
+  ptx::griddep_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_last();  // both operands are re-read by other CTAs
+      int issued = 0;
+      for (int k = 0; k < ksteps; ++k) {
+        const int st = k % kRtStages;
+        const uint32_t ph = (k / kRtStages) & 1;
+        if (!wait_bar(&empty[st], ph ^ 1u, abort_flag, 20, kTimeoutNs)) break;
+        uint8_t* s = tiles + st * kStage;
+        ptx::mbar_arrive_expect_tx(&full[st], kStage);
+        ptx::tma_load_3d(s, &tmap_w3, &full[st], k * kBK, m0, 0, pol);
+        ptx::tma_load_2d(s + kA, &tmap_z, &full[st], k * kBK, n0, pol);
+        ++issued;
+      }
+      if (issued < ksteps) {
+        // unwinding: let the copies already in flight land before the CTA exits
+        for (int i = issued > kRtStages ? issued - kRtStages : 0; i < issued; ++i)
+          wait_bar(&full[i % kRtStages], (i / kRtStages) & 1, nullptr, 23, kDrainNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, BN);
+      for (int k = 0; k < ksteps; ++k) {
+        const int st = k % kRtStages;
+        const int b = k & 1;
+        if (!wait_bar(&tempty[b], ((k >> 1) & 1) ^ 1u, abort_flag, 24, kTimeoutNs)) break;
+        if (!wait_bar(&full[st], (k / kRtStages) & 1, abort_flag, 21, kTimeoutNs)) break;
+        ptx::tc_fence_after();
+        const uint32_t a = ptx::smem_u32(tiles + st * kStage);
+        const uint32_t bt = a + kA;
+        const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+#pragma unroll
+        for (int s = 0; s < 3; ++s)
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j)
+            ptx::mma_bf16(d, ptx::smem_desc_k128(a + s * kTileABytes + j * 32), ptx::smem_desc_k128(bt + j * 32),
+                          idesc, (s > 0 || j > 0) ? 1u : 0u);
+        ptx::mma_commit(&empty[st]);
+        ptx::mma_commit(&tfull[b]);
+      }
+    }
+  } else {
+    const int sub = warp & 3;
+    const int e = m0 + sub * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    float acc[BN];
+#pragma unroll
+    for (int i = 0; i < BN; ++i) acc[i] = 0.f;
+    bool ok = true;
+    for (int k = 0; k < ksteps && ok; ++k) {
+      const int b = k & 1;
+      if (!wait_bar(&tfull[b], (k >> 1) & 1, abort_flag, 22, kTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        ptx::tmem_ld16(lane_base + static_cast<uint32_t>(b * BN + c0), r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[c0 + j] = __fadd_rn(acc[c0 + j], __uint_as_float(r[j]));
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[b]);
+    }
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < BN; ++i) {
+        const int t = n0 + i;
+        if (t < T && e < E) logits[static_cast<size_t>(t) * E + e] = acc[i];
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kCols);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeFn = decltype(&cuTensorMapEncodeTiled);
 
@@ -1065,6 +1225,59 @@ cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t
                                         reinterpret_cast<uint4*>(y));
   ++launch_counter();
   return err;
+}
+
+namespace {
+
+template <int BN>
+cudaError_t launch_router_tc_bn(const CUtensorMap& mw, const CUtensorMap& mz, int T, int E, int H, float* logits,
+                                cudaStream_t stream, bool pdl) {
+  constexpr int kSmem = 1024 + kRtStages * (3 * kTileABytes + BN * kBK * 2);
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(router_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const dim3 grid((T + BN - 1) / BN, E / kBM);
+  const cudaError_t err =
+      launch_kernel(router_tc_kernel<BN>, grid, dim3(kRtThreads), kSmem, stream, pdl, mw, mz, T, E, H / kBK, logits);
+  ++launch_counter();
+  return err;
+}
+
+}  // namespace
+
+bool router_tc_supported(int T, int E, int H) { return T > 128 && E % kBM == 0 && E <= 256 && H % kBK == 0; }
+
+size_t router_tc_scratch_bytes(int E, int H) { return 3 * static_cast<size_t>(E) * H * sizeof(uint16_t); }
+
+cudaError_t launch_router_tc(const uint16_t* z, const float* W, int T, int E, int H, float* logits, uint16_t* w3,
+                             int num_sms, cudaStream_t stream, bool pdl) {
+  const size_t n = static_cast<size_t>(E) * H;
+  cudaError_t err = launch_kernel(split_router_weights_kernel, dim3(num_sms * 4), dim3(256), 0, stream, pdl, W, w3, n);
+  ++launch_counter();
+  if (err != cudaSuccess) return err;
+  // the weight terms as a 3-D tensor (k, expert, term), the tokens as 2-D (k, token)
+  CUtensorMap mw, mz;
+  const cuuint64_t dw[3] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(E), 3};
+  const cuuint64_t sw[2] = {static_cast<cuuint64_t>(H) * 2, static_cast<cuuint64_t>(E) * H * 2};
+  const cuuint32_t bw[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM), 3};
+  if (!encode_map(&mw, w3, 3, dw, sw, bw)) return cudaErrorInvalidValue;
+  // token tile: the widest of 128/64/32 that still gives at least one CTA per SM
+  int bn = 128;
+  while (bn > 32 && ((T + bn - 1) / bn) * (E / kBM) < num_sms) bn >>= 1;
+  const cuuint64_t dz[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  const cuuint64_t sz[1] = {static_cast<cuuint64_t>(H) * 2};
+  const cuuint32_t bz[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(bn)};
+  if (!encode_map(&mz, z, 2, dz, sz, bz)) return cudaErrorInvalidValue;
+  switch (bn) {
+    case 128: return launch_router_tc_bn<128>(mw, mz, T, E, H, logits, stream, pdl);
+    case 64: return launch_router_tc_bn<64>(mw, mz, T, E, H, logits, stream, pdl);
+    default: return launch_router_tc_bn<32>(mw, mz, T, E, H, logits, stream, pdl);
+  }
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream) {

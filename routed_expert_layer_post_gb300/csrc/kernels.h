@@ -31,6 +31,12 @@ bool router_topk_fusable(int T, int E, int G);
 cudaError_t launch_router_topk_fused(const uint16_t* z, const float* W, const float* bias, int T, int H, int E,
                                      int G, int TG, int K, float scale, float* logits, int32_t* ids, float* w,
                                      int* ticket, cudaStream_t stream, bool pdl);
+// Tensor-core FP32 router for T > 128: splits W exactly into three bf16 terms
+// (`w3`, router_tc_scratch_bytes) and accumulates all three in fp32.
+bool router_tc_supported(int T, int E, int H);
+size_t router_tc_scratch_bytes(int E, int H);
+cudaError_t launch_router_tc(const uint16_t* z, const float* W, int T, int E, int H, float* logits, uint16_t* w3,
+                             int num_sms, cudaStream_t stream, bool pdl);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int G, int TG, int K, float scale,
                         int32_t* ids, float* w, cudaStream_t stream, bool pdl = false);
 

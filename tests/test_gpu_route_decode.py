@@ -59,6 +59,12 @@ def test_fused_routing_matches_staged_path_and_oracle(T):
     assert np.array_equal(np.diff(dbg["expert_offsets"].cpu().numpy()), counts)
     mx, rel = layer_errors(f64_of(y)[same], ref["y"][same])
     assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
+    # the experts and combine stages give the same bits as the separate
+    # experts entry point on the layer's own routing
+    offs2, _, inv2, xp2 = beam.beam_moe_permute(dbg["topk_ids"], dbg["z"], m.mc)
+    y2 = beam.beam_moe_experts(xp2, offs2, m.dev[0], m.dev[1], dbg["topk_w"], inv2, m.mc, T)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
 @pytest.mark.parametrize("T", [1, 8])
