@@ -214,6 +214,17 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
  * out, otherwise a nonzero site code; returns BEAM_ERR_DEVICE_TIMEOUT then. */
 beam_status_t beam_get_device_error(int* code, void* stream);
 
+/* Diagnostic with no counterpart in the pages: checks on the device that a
+ * bounded wait gives up and reports instead of hanging. One thread waits,
+ * through the same wait routine the fused experts launch uses for its
+ * cross-CTA counters and routing flags, on a flag that nothing sets, for
+ * `limit_ms` (1..1000) milliseconds. `flag`: 4 writable device bytes, 4-byte
+ * aligned, zeroed here. Synchronises `stream`; the error word is cleared
+ * before returning. Returns BEAM_OK when the wait timed out and reported its
+ * site code (*site receives it), BEAM_ERR_DEVICE_TIMEOUT if another site code
+ * was pending or none was recorded, BEAM_ERR_INVALID_ARG on bad arguments. */
+beam_status_t beam_check_bounded_wait(int* flag, int limit_ms, int* site, void* stream);
+
 /* Kernel launches issued by the most recent call of each kind on this host
  * thread's view (a count, for reporting). */
 int beam_last_launch_count(void);

@@ -503,4 +503,23 @@ beam_status_t beam_get_device_error(int* code, void* stream) {
   return *code != 0 ? BEAM_ERR_DEVICE_TIMEOUT : BEAM_OK;
 }
 
+beam_status_t beam_check_bounded_wait(int* flag, int limit_ms, int* site, void* stream) {
+  if (flag == nullptr || site == nullptr || limit_ms < 1 || limit_ms > 1000 || !aligned4(flag))
+    return BEAM_ERR_INVALID_ARG;
+  *site = 0;
+  DeviceInfo d;
+  beam_status_t st = device_info(&d);
+  if (st != BEAM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int pending = 0;
+  if (beam::read_and_clear_device_error(&pending, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  if (pending != 0) return BEAM_ERR_DEVICE_TIMEOUT;
+  launch_counter() = 0;
+  if (beam::launch_bounded_wait_probe(flag, static_cast<uint64_t>(limit_ms) * 1000000ull, beam::kProbeSite, s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  if (beam::read_and_clear_device_error(site, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  return *site == beam::kProbeSite ? BEAM_OK : BEAM_ERR_DEVICE_TIMEOUT;
+}
+
 }  // extern "C"

@@ -160,7 +160,8 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 }
 
 // Wait (bounded) until *counter >= target; other CTAs of this launch raise it.
-__device__ __forceinline__ bool wait_counter(const int* counter, int target, volatile int* abort_flag, int site) {
+__device__ __forceinline__ bool wait_counter(const int* counter, int target, volatile int* abort_flag, int site,
+                                             uint64_t limit_ns = kTimeoutNs) {
   if (ld_acquire(counter) >= target) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -168,7 +169,7 @@ __device__ __forceinline__ bool wait_counter(const int* counter, int target, vol
     if (ld_acquire(counter) >= target) return true;
     if ((it & 15u) == 0) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      if (ptx::globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicCAS(&g_device_error, 0, site);
         return false;
@@ -805,6 +806,16 @@ __global__ void __launch_bounds__(256)
   y[idx] = pack8(acc);
 }
 
+// ------------------------------------------------------------------ bounded-wait check
+// One thread waits, through the same bounded wait the fused launch uses for
+// its cross-CTA counters and routing flags, on a flag that nothing sets: it
+// must give up after `limit_ns`, record `site` and return.
+__global__ void bounded_wait_probe_kernel(const int* flag, uint64_t limit_ns, int site) {
+  __shared__ int abort_s;
+  abort_s = 0;
+  wait_counter(flag, 1, &abort_s, site, limit_ns);
+}
+
 // ------------------------------------------------------------------ tensor-core FP32 router
 // logits[t][e] = sum_k z[t][k] * W[e][k] for prefill sizes. Each fp32 weight
 // is split exactly into three bf16 terms, W = hi + mid + lo (hi = bf16(W),
@@ -1278,6 +1289,14 @@ cudaError_t launch_router_tc(const uint16_t* z, const float* W, int T, int E, in
     case 64: return launch_router_tc_bn<64>(mw, mz, T, E, H, logits, stream, pdl);
     default: return launch_router_tc_bn<32>(mw, mz, T, E, H, logits, stream, pdl);
   }
+}
+
+cudaError_t launch_bounded_wait_probe(int* flag, uint64_t limit_ns, int site, cudaStream_t stream) {
+  cudaError_t err = cudaMemsetAsync(flag, 0, sizeof(int), stream);
+  if (err != cudaSuccess) return err;
+  bounded_wait_probe_kernel<<<1, 1, 0, stream>>>(flag, limit_ns, site);
+  ++launch_counter();
+  return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream) {

@@ -98,5 +98,8 @@ cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down,
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,
                            uint16_t* y, cudaStream_t stream, bool pdl = false);
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream);
+// One bounded wait on `flag` (zeroed here) that nothing sets: records `site`.
+constexpr int kProbeSite = 99;
+cudaError_t launch_bounded_wait_probe(int* flag, uint64_t limit_ns, int site, cudaStream_t stream);
 
 }  // namespace beam

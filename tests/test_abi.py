@@ -115,3 +115,12 @@ def test_workspace_sizes_grow_with_tokens(beam):
     T = 2048
     assert sizes[2] >= T * 8 * (2 * 5120 + 2560) * 2
     assert lib.beam_moe_layer_host_workspace_size(ctypes.byref(c), T) >= sizes[2] + 4 * T * 5120 * 2
+
+
+def test_bounded_wait_check_rejects_bad_arguments(beam):
+    lib = beam.library()
+    site = ctypes.c_int(7)
+    assert lib.beam_check_bounded_wait(None, 50, ctypes.byref(site), None) == 1
+    assert lib.beam_check_bounded_wait(ctypes.c_void_p(256), 0, ctypes.byref(site), None) == 1
+    assert lib.beam_check_bounded_wait(ctypes.c_void_p(256), 5000, ctypes.byref(site), None) == 1
+    assert lib.beam_check_bounded_wait(ctypes.c_void_p(258), 50, ctypes.byref(site), None) == 1  # misaligned
