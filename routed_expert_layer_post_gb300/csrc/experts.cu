@@ -186,14 +186,20 @@ struct Unit {
 
 // Tiles of a phase are laid out expert by expert, row block by row block,
 // token tile fastest; expert e's tiles start at n_mb * s_ttstart[e].
+// `rot0` (fused launch): phase-0 tiles are taken starting at tile rot0 (an
+// expert boundary), wrapping around at n_tiles0.
 __device__ __forceinline__ Unit decode_unit(int u, int n_units0, const GemmParams& p, const int* s_ttstart,
-                                            const int* s_ntt) {
+                                            const int* s_ntt, int rot0 = 0, int n_tiles0 = 0) {
   Unit r;
   r.phase = (u < n_units0) ? 0 : 1;
   const PhaseParams& ph = p.ph[r.phase];
   const int v = r.phase == 0 ? u : u - n_units0;
   r.tile = v / ph.split;
   r.s = v - r.tile * ph.split;
+  if (r.phase == 0 && rot0 != 0) {
+    r.tile += rot0;
+    if (r.tile >= n_tiles0) r.tile -= n_tiles0;
+  }
   const int q = r.tile / ph.n_mb;
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
@@ -346,6 +352,24 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   }
   if (MODE == 2 && s_flags[2]) n_tiles0 = 0;  // the routing flags never came: do nothing
   const int n_units0 = n_tiles0 * p.ph[0].split;
+  // Fused launch: the first wave of gate/up units goes to the last experts.
+  // Their epilogues run first on every SM, with cold instructions under full
+  // HBM load, and finish late; the down units of those experts come last, so
+  // nothing waits on them. rot0 is the start of the earliest expert such that
+  // the experts from it to the end hold at least one wave of units.
+  int rot0 = 0;
+  if (MODE == 2 && n_tiles0 > 0) {
+    const int wave_tiles = (static_cast<int>(gridDim.x) + p.ph[0].split - 1) / p.ph[0].split;
+    const int limit = n_tiles0 - wave_tiles;
+    if (limit > 0) {
+      int lo = 0, hi = p.E - 1;  // largest e with n_mb * s_ttstart[e] <= limit
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.ph[0].n_mb * s_ttstart[mid] <= limit) lo = mid; else hi = mid - 1;
+      }
+      rot0 = p.ph[0].n_mb * s_ttstart[lo];
+    }
+  }
   int n_units = n_units0;
   if (MODE == 2 && n_tiles0 > 0) {
     const int n_tiles1 = n_tt * p.ph[1].n_mb;
@@ -436,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         }
         // ask for the following unit now: the atomic's round trip overlaps this unit's loads
         u_next = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
-        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
+        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
         const int nacc = kind == 0 ? 2 : 1;
@@ -550,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         if (wait_bar(&qfull[slot], (seq / kQueue) & 1, abort_flag, 6, kTimeoutNs)) u = s_queue[slot];
         ptx::mbar_arrive(&qempty[slot]);
         if (u < 0) break;
-        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
+        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
         const int nacc = kind == 0 ? 2 : 1;
@@ -637,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       ptx::named_bar_sync(bar_id, 128);
       if (u < 0) break;
       ptx::tc_fence_after();
-      const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt);
+      const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
       const PhaseParams& ph = p.ph[w.phase];
       const int kind = unit_kind<MODE>(w.phase);
       const int nacc = kind == 0 ? 2 : 1;
@@ -693,47 +717,40 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         ptx::named_bar_sync(bar_id, 128);
         const int last = *reinterpret_cast<volatile int*>(&g_flags[1]);
         if (last) {
+          // One output column at a time: partials requested eight splits at a
+          // time and summed in split order (the result does not depend on
+          // timing), then SwiGLU or the plain value, one store. The loops stay
+          // rolled: this path runs once per tile at decode sizes (a handful of
+          // columns), and its first run on an SM fetches its instructions
+          // while HBM is saturated, so its size is its cost.
           const float* tile_parts = ph.partials + static_cast<size_t>(w.tile) * ph.split * slot_elems;
-          for (int c0 = 0; c0 < valid; c0 += 16) {
-            float v[2][16];
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[a][j] = 0.f;
-            for (int j = 0; j < 16 && c0 + j < valid; ++j) {
-              // partials are requested eight splits at a time and summed in
-              // split order (the result does not depend on timing). The loop
-              // stays rolled: this path runs once per tile, and its first run
-              // on an SM fetches its instructions while HBM is saturated.
-              float sum[C::kNAcc];
-#pragma unroll
-              for (int a = 0; a < C::kNAcc; ++a) sum[a] = 0.f;
 #pragma unroll 1
-              for (int s0 = 0; s0 < ph.split; s0 += 8) {
-                float x[C::kNAcc][8];
+          for (int j = 0; j < valid; ++j) {
+            float g = 0.f, u2 = 0.f;
+            const size_t off0 = static_cast<size_t>(j) * kBM + m;
+            const size_t off1 = static_cast<size_t>(BN + j) * kBM + m;
+#pragma unroll 1
+            for (int s0 = 0; s0 < ph.split; s0 += 8) {
+              float x0[8], x1[8];
 #pragma unroll
-                for (int a = 0; a < C::kNAcc; ++a) {
-                  const size_t off = static_cast<size_t>(a * BN + c0 + j) * kBM + m;
-#pragma unroll
-                  for (int i = 0; i < 8; ++i)
-                    x[a][i] = (a < nacc && s0 + i < ph.split) ? __ldcg(tile_parts + (s0 + i) * slot_elems + off)
-                                                               : 0.f;
-                }
-#pragma unroll
-                for (int a = 0; a < C::kNAcc; ++a)
-#pragma unroll
-                  for (int i = 0; i < 8; ++i)
-                    if (s0 + i < ph.split) sum[a] = (s0 + i == 0) ? x[a][i] : sum[a] + x[a][i];
+              for (int i = 0; i < 8; ++i) {
+                const bool in = s0 + i < ph.split;
+                x0[i] = in ? __ldcg(tile_parts + (s0 + i) * slot_elems + off0) : 0.f;
+                x1[i] = (in && nacc > 1) ? __ldcg(tile_parts + (s0 + i) * slot_elems + off1) : 0.f;
               }
 #pragma unroll
-              for (int a = 0; a < C::kNAcc; ++a) {
-                if (a >= nacc) continue;
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                  if (jj == j) v[a][jj] = sum[a];
+              for (int i = 0; i < 8; ++i) {
+                if (s0 + i < ph.split) {
+                  g = (s0 + i == 0) ? x0[i] : g + x0[i];
+                  u2 = (s0 + i == 0) ? x1[i] : u2 + x1[i];
+                }
               }
             }
-            store_outputs<BN>(ph, p.rows, kind, v, c0, valid, row0, col);
+            const int row = row0 + j;
+            if (row >= 0 && row < p.rows) {
+              const float val = kind == 0 ? g / (1.0f + __expf(-g)) * u2 : g;
+              ph.out[static_cast<size_t>(row) * ph.out_ld + col] = static_cast<uint16_t>(f2bf(val));
+            }
           }
           if (leader) ph.tickets[w.tile] = 0;
           tile_done = true;
