@@ -120,3 +120,30 @@ def test_empty_batch():
     e = torch.empty(0, m.cfg.H, dtype=torch.bfloat16, device="cuda")
     h_out, y, _ = beam.beam_moe_layer(e, e.clone(), 3, m.weights, m.mc)
     assert y.shape == (0, m.cfg.H)
+
+
+def test_skewed_routing_several_token_tiles_per_expert():
+    # 32 of 64 tokens are copies of one token, so its 8 experts each receive
+    # 32+ rows: several 16-row token tiles per expert inside the fused launch
+    # (the down units of a token tile wait for all of that tile's gate/up rows)
+    from beam_inputs import make_activations
+    m = model("decode_t64")
+    cfg = m.cfg.with_(T=64)
+    hb, xb = make_activations(cfg, batch=500)
+    hb[:32] = hb[0]
+    xb[:32] = xb[0]
+    h_out, y, dbg = run_layer(m, dev_bf16(hb), dev_bf16(xb))
+    ids = dbg["topk_ids"].cpu().numpy()
+    counts = np.diff(dbg["expert_offsets"].cpu().numpy())
+    assert counts[ids[0]].min() >= 32
+    yb = bits_of(y)
+    assert all(np.array_equal(yb[t], yb[0]) for t in range(1, 32))  # identical rows, identical bits
+    from oracle.layer import layer
+    tokens = np.array([0, 31, 32, 45, 63])
+    ref = layer(obf.decode(hb), obf.decode(xb), obf.decode(m.wp_bits), obf.decode(m.wq_bits), m.W_r, m.bias,
+                n=cfg.n, eps=cfg.eps, G=cfg.G, TG=cfg.TG, K=cfg.K, routed_scale=cfg.routed_scale,
+                expert_fn=m.expert_fn_nocache, tokens=tokens, workers=16)
+    same = np.all(ids[tokens] == ref["ids"], axis=1)
+    assert np.all(same | near_tie(ref["route"]))
+    mx, rel = layer_errors(f64_of(y)[tokens][same], ref["y"][same])
+    assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
