@@ -488,9 +488,14 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
     else:
+        # a contraction timed inside a step of more than a millisecond runs at
+        # the power-capped (sustained) rate, so it is measured against that peak
+        long_step = statistics.fmean(staged_step_ms) > 1.0
+        peak_key = "bf16_tflops_sustained" if long_step and "bf16_tflops_sustained" in peaks else "bf16_tflops"
+        peaks_kind = f"{peaks_kind} {'sustained' if peak_key.endswith('sustained') else 'burst'}"
         achieved = flops * K2 / dom_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"]}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks[peak_key], "unit": "TFLOP/s",
+                "frac": achieved / peaks[peak_key]}
     roof.update({"traffic": profiled_traffic(dom, cfg.name), "kernel": dom, "peak_source": peaks_kind,
                  "algorithmic_bytes_per_launch": bytes_total / K2,
                  "launch_us": 1e3 * statistics.fmean(stage_ms[dom_stage]),
