@@ -202,7 +202,12 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n,
 /* beam_moe_layer with HOST input and output buffers: copies h and x (host,
  * pinned memory recommended) into the workspace, runs the layer, copies h_out
  * and y_out back to the host buffers, and synchronises the stream before it
- * returns. Weights stay device pointers. Workspace: beam_moe_layer_host_workspace_size. */
+ * returns. Up to 8 tokens, when all four host buffers are page-locked (mapped
+ * into the device address space) and 16-byte aligned, one kernel reads h and x
+ * from the mapped memory and the layer writes h_out and y_out to it directly
+ * instead of four copy-engine transfers; the results are the same bits. h_out
+ * must not alias x; y_out must alias none of the others. Weights stay device
+ * pointers. Workspace: beam_moe_layer_host_workspace_size. */
 size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T);
 beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
                                   const beam_moe_weights_t* weights, int T,

@@ -467,6 +467,29 @@ size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T) {
   return base + 4 * act;
 }
 
+namespace {
+
+// Device-visible address of a page-locked host buffer, or nullptr.
+void* mapped_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// h and x from mapped host memory into the device workspace in one launch.
+__global__ void stage_in_kernel(const uint4* __restrict__ h, const uint4* __restrict__ x, uint4* __restrict__ dh,
+                                uint4* __restrict__ dx, int n16) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x) {
+    dh[i] = h[i];
+    dx[i] = x[i];
+  }
+}
+
+}  // namespace
+
 beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
                                   const beam_moe_weights_t* wt, int T, const beam_moe_config_t* cfg,
                                   uint16_t* h_out_host, uint16_t* y_out_host, void* ws, size_t ws_bytes,
@@ -487,6 +510,28 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
   uint16_t* d_hn = reinterpret_cast<uint16_t*>(base + 2 * act);
   uint16_t* d_y = reinterpret_cast<uint16_t*>(base + 3 * act);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Decode sizes with page-locked buffers: one kernel reads h and x from the
+  // mapped host memory and the layer writes h' and y straight to the host
+  // buffers, instead of four copy-engine transfers (about 18 us at 1 token).
+  if (T <= 8) {
+    void* mh = mapped_host(h_host);
+    void* mx = mapped_host(x_host);
+    void* mho = mapped_host(h_out_host);
+    void* myo = mapped_host(y_out_host);
+    if (mh && mx && mho && myo && aligned16(mh) && aligned16(mx) && aligned16(mho) && aligned16(myo) &&
+        mho != mx && myo != mh && myo != mx && myo != mho) {
+      const int n16 = static_cast<int>(bytes / 16);
+      stage_in_kernel<<<(n16 + 255) / 256, 256, 0, s>>>(static_cast<const uint4*>(mh), static_cast<const uint4*>(mx),
+                                                      reinterpret_cast<uint4*>(d_h), reinterpret_cast<uint4*>(d_x),
+                                                      n16);
+      if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+      st = beam_moe_layer(d_h, d_x, n, wt, T, cfg, static_cast<uint16_t*>(mho), static_cast<uint16_t*>(myo),
+                          nullptr, base + 4 * act, ws_bytes - 4 * act, stream);
+      if (st != BEAM_OK) return st;
+      launch_counter() += 1;
+      return cuda_status(cudaStreamSynchronize(s));
+    }
+  }
   if (cudaMemcpyAsync(d_h, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaMemcpyAsync(d_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
   st = beam_moe_layer(d_h, d_x, n, wt, T, cfg, d_hn, d_y, nullptr, base + 4 * act, ws_bytes - 4 * act, stream);

@@ -104,14 +104,25 @@ def test_all_tokens_on_one_group():
     assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
 
 
-def test_host_buffer_entry_point_matches_device_entry_point():
+@pytest.mark.parametrize("T,pinned_out", [(1, True), (1, False), (8, True), (16, True)])
+def test_host_buffer_entry_point_matches_device_entry_point(T, pinned_out):
+    # up to 8 tokens with page-locked buffers the layer reads and writes the
+    # mapped host memory directly; otherwise it copies in and out
+    from beam_inputs import make_activations
     beam = beam_module()
-    m = model("decode_t1")
-    _, y_dev, _ = run_layer(m)
-    h_host = torch.from_numpy(m.h_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    x_host = torch.from_numpy(m.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_out, y = beam.beam_moe_layer_host(h_host, x_host, m.cfg.n, m.weights, m.mc)
-    assert torch.equal(y, y_dev.cpu())
+    m = model("decode_t64")
+    cfg = m.cfg.with_(T=T)
+    hb, xb = make_activations(cfg, batch=600 + T)
+    h_dev, y_dev, _ = run_layer(m, dev_bf16(hb), dev_bf16(xb), n=cfg.n)
+    h_host = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty_like(h_host)
+    y_out = torch.empty_like(h_host)
+    if pinned_out:
+        h_out, y_out = h_out.pin_memory(), y_out.pin_memory()
+    h_out, y = beam.beam_moe_layer_host(h_host, x_host, cfg.n, m.weights, m.mc, h_out_host=h_out, y_out_host=y_out)
+    assert torch.equal(y.view(torch.int16), y_dev.cpu().view(torch.int16))
+    assert torch.equal(h_out.view(torch.int16), h_dev.cpu().view(torch.int16))
 
 
 def test_empty_batch():
