@@ -63,13 +63,13 @@ __global__ void __launch_bounds__(1024)
   const uint4 hv = h[idx];
   const uint4 wp = w_post[c];
   const uint4 wq = w_pre[c];
-  F2 acc{0.f, 0.f};
-  acc_squares(acc, xv);
-  const F2 r = block_rsqrt_mean(acc, red, nwarps, inv_h, eps);
-  F2 acc2{0.f, 0.f};
+  F2x2 acc{{0.f, 0.f}, {0.f, 0.f}};
+  acc_squares2(acc, xv);
+  const F2 r = block_rsqrt_mean(fold(acc), red, nwarps, inv_h, eps);
+  F2x2 acc2{{0.f, 0.f}, {0.f, 0.f}};
   const uint4 hn = chunk_residual(xv, hv, wp, r, coef, acc2);
   h_out[idx] = hn;
-  const F2 r2 = block_rsqrt_mean(acc2, red, nwarps, inv_h, eps);
+  const F2 r2 = block_rsqrt_mean(fold(acc2), red, nwarps, inv_h, eps);
   z_out[idx] = chunk_scale(hn, wq, r2);
 }
 

@@ -783,9 +783,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 
 // ------------------------------------------------------------------ combine
 // y[t] = bf16(sum_k w[t][k] * y_perm[inv_perm[t*K+k]]), k in slot order, one
-// thread per 8 hidden columns of a token; no atomics.
+// thread per 8 hidden columns of a token; no atomics. KMAX bounds K: the
+// register arrays hold KMAX rows, so K <= 8 (Beam) keeps registers low enough
+// for four blocks per SM (the kernel is latency-bound on the row loads).
 constexpr int kMaxTopK = 16;
 
+template <int KMAX>
 __global__ void __launch_bounds__(256)
     combine_kernel(const uint4* __restrict__ y_perm, const float* __restrict__ w, const int32_t* __restrict__ inv,
                    int T, int K, int chunks, uint4* __restrict__ y) {
@@ -796,10 +799,10 @@ __global__ void __launch_bounds__(256)
   const int t = static_cast<int>(idx / chunks);
   const int c = static_cast<int>(idx - static_cast<size_t>(t) * chunks);
   // all K rows are requested before the first one is used
-  uint4 rows[kMaxTopK];
-  float wk[kMaxTopK];
+  uint4 rows[KMAX];
+  float wk[KMAX];
 #pragma unroll
-  for (int k = 0; k < kMaxTopK; ++k) {
+  for (int k = 0; k < KMAX; ++k) {
     rows[k] = make_uint4(0u, 0u, 0u, 0u);
     wk[k] = 0.f;
     if (k < K) {
@@ -812,7 +815,7 @@ __global__ void __launch_bounds__(256)
   }
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int k = 0; k < kMaxTopK; ++k) {
+  for (int k = 0; k < KMAX; ++k) {
     if (k < K) {
       float f[8];
       unpack8(rows[k], f);
@@ -1248,7 +1251,8 @@ cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t
   const int chunks = H / 8;
   const size_t n = static_cast<size_t>(T) * chunks;
   const int blocks = static_cast<int>((n + 255) / 256);
-  const cudaError_t err = launch_kernel(combine_kernel, dim3(blocks), dim3(256), 0, stream, pdl,
+  const cudaError_t err = launch_kernel(K <= 8 ? combine_kernel<8> : combine_kernel<kMaxTopK>, dim3(blocks),
+                                        dim3(256), 0, stream, pdl,
                                         reinterpret_cast<const uint4*>(y_perm), w, inv_perm, T, K, chunks,
                                         reinterpret_cast<uint4*>(y));
   ++launch_counter();

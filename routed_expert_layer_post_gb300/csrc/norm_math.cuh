@@ -23,12 +23,6 @@ __device__ __forceinline__ F2 two_sum(float a, float b) {
   return {s, e};
 }
 
-__device__ __forceinline__ void acc_add(F2& acc, float v) {
-  const F2 t = two_sum(acc.hi, v);
-  acc.hi = t.hi;
-  acc.lo = __fadd_rn(acc.lo, t.lo);
-}
-
 // symmetric in its arguments, so butterfly reductions agree bit for bit on every lane
 __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
   const F2 t = two_sum(a.hi, b.hi);
@@ -122,64 +116,114 @@ __device__ __forceinline__ uint32_t residual_bf16(float h, float y, const Residu
   return round_pair(v_hi, __fsub_rn(ve, __fsub_rn(v_hi, v)));
 }
 
-__device__ __forceinline__ void acc_squares(F2& acc, const uint4& v) {
-  float f[8];
-  unpack8(v, f);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc_add(acc, __fmul_rn(f[i], f[i]));  // exact square of a bf16 value
-}
-
 // Adaptive precision: the plain fp32 value v is used when every value within
 // its error bound e rounds to the same bf16 number (the usual case); only
 // values whose interval [v - e, v + e] straddles a rounding midpoint take the
-// exact double-float path above. The bounds are deliberately loose (about
+// exact double-float paths above. The bounds are deliberately loose (about
 // four times the worst-case fp32 error), so the fast path never decides a
 // case the exact path would decide differently.
-__device__ __forceinline__ bool rounds_alike(float v, float e) {
-  return f2bf(__fsub_rn(v, e)) == f2bf(__fadd_rn(v, e));
+//
+// The fast paths and the sums of squares work on element pairs with
+// Blackwell's packed fp32 arithmetic: each lane of __fmul2_rn / __fadd2_rn /
+// __ffma2_rn is one IEEE round-to-nearest operation, the value of the scalar
+// form, at half the issue slots (the boundary is issue-bound). An element
+// whose rounding the check leaves open falls back alone to the exact path.
+
+__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+__device__ __forceinline__ float2 abs2(float2 v) { return make_float2(fabsf(v.x), fabsf(v.y)); }
+
+// bf16x2 bits (element 0 in the low half) of a pair
+__device__ __forceinline__ uint32_t bf16x2_bits(float2 v) {
+  const __nv_bfloat162 b = __float22bfloat162_rn(v);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// bf16(a * b * r), a and b bf16 values, r a pair with |r.lo| <= 2^-24 |r.hi|
-__device__ __forceinline__ uint32_t scaled_bf16_fast(float a, float b, const F2& r) {
-  const float v = __fmul_rn(__fmul_rn(a, b), r.hi);  // a * b is exact
-  if (rounds_alike(v, fabsf(v) * 0x1p-21f)) return f2bf(v);
-  return scaled_bf16(a, b, r);
+// Pair of double-float accumulators (element 0 and element 1 sums)
+struct F2x2 {
+  float2 hi, lo;
+};
+
+__device__ __forceinline__ void acc_add2(F2x2& acc, float2 v) {
+  const float2 s = __fadd2_rn(acc.hi, v);
+  const float2 bp = __fadd2_rn(s, neg2(acc.hi));
+  const float2 e = __fadd2_rn(__fadd2_rn(acc.hi, neg2(__fadd2_rn(s, neg2(bp)))), __fadd2_rn(v, neg2(bp)));
+  acc.hi = s;
+  acc.lo = __fadd2_rn(acc.lo, e);
 }
 
-// bf16((sqrt(n-1) h + y) / sqrt(n)); the error of the fp32 evaluation is
-// bounded by a few ulps of c * (|sqrt(n-1) h| + |y|), which covers cancellation
-__device__ __forceinline__ uint32_t residual_bf16_fast(float h, float y, const ResidualCoef& k) {
-  const float ch = __fmul_rn(k.cm_hi, h);
-  const float v = __fmul_rn(fmaf(k.cm_hi, h, y), k.c_hi);
-  const float e = __fmul_rn(__fadd_rn(fabsf(ch), fabsf(y)), k.c_hi) * 0x1p-20f;
-  if (rounds_alike(v, e)) return f2bf(v);
-  return residual_bf16(h, y, k);
+// the two lanes' sums as one pair
+__device__ __forceinline__ F2 fold(const F2x2& a) { return f2_add(F2{a.hi.x, a.lo.x}, F2{a.hi.y, a.lo.y}); }
+
+// bf16x2 of a * b * r for a pair: a, b bf16 values (a * b exact in fp32), r a
+// pair with |r.lo| <= 2^-24 |r.hi|, so v = fl(a b r.hi) is within about
+// |v| 2^-23 of the exact value (the check allows |v| 2^-21)
+__device__ __forceinline__ uint32_t scaled_bf16x2_fast(float2 a, float2 b, const F2& r) {
+  const float2 v = __fmul2_rn(__fmul2_rn(a, b), make_float2(r.hi, r.hi));
+  const float2 e = __fmul2_rn(abs2(v), make_float2(0x1p-21f, 0x1p-21f));
+  const uint32_t lo = bf16x2_bits(__fadd2_rn(v, neg2(e)));
+  const uint32_t hi = bf16x2_bits(__fadd2_rn(v, e));
+  if (lo == hi) return bf16x2_bits(v);
+  uint32_t out = 0;
+  out |= ((lo & 0xffffu) == (hi & 0xffffu)) ? f2bf(v.x) : scaled_bf16(a.x, b.x, r);
+  out |= (((lo >> 16) == (hi >> 16)) ? f2bf(v.y) : scaled_bf16(a.y, b.y, r)) << 16;
+  return out;
+}
+
+// bf16x2 of (sqrt(n-1) h + y) / sqrt(n) for a pair; the error of the fp32
+// evaluation is bounded by a few ulps of c (|sqrt(n-1) h| + |y|), which covers
+// cancellation
+__device__ __forceinline__ uint32_t residual_bf16x2_fast(float2 h, float2 y, const ResidualCoef& k) {
+  const float2 cm = make_float2(k.cm_hi, k.cm_hi), c = make_float2(k.c_hi, k.c_hi);
+  const float2 ch = __fmul2_rn(cm, h);
+  const float2 v = __fmul2_rn(__ffma2_rn(cm, h, y), c);
+  const float2 e =
+      __fmul2_rn(__fmul2_rn(__fadd2_rn(abs2(ch), abs2(y)), c), make_float2(0x1p-20f, 0x1p-20f));
+  const uint32_t lo = bf16x2_bits(__fadd2_rn(v, neg2(e)));
+  const uint32_t hi = bf16x2_bits(__fadd2_rn(v, e));
+  if (lo == hi) return bf16x2_bits(v);
+  uint32_t out = 0;
+  out |= ((lo & 0xffffu) == (hi & 0xffffu)) ? f2bf(v.x) : residual_bf16(h.x, y.x, k);
+  out |= (((lo >> 16) == (hi >> 16)) ? f2bf(v.y) : residual_bf16(h.y, y.y, k)) << 16;
+  return out;
+}
+
+__device__ __forceinline__ void acc_squares2(F2x2& acc, const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
+    acc_add2(acc, __fmul2_rn(f, f));  // exact squares of bf16 values
+  }
 }
 
 // y and h' for one 8-element chunk; returns h' packed, accumulates its squares
 __device__ __forceinline__ uint4 chunk_residual(const uint4& xv, const uint4& hv, const uint4& wv, const F2& r,
-                                                const ResidualCoef& coef, F2& acc) {
-  float fx[8], fh[8], fw[8], hn[8];
-  unpack8(xv, fx);
-  unpack8(hv, fh);
-  unpack8(wv, fw);
+                                                const ResidualCoef& coef, F2x2& acc) {
+  const uint32_t x[4] = {xv.x, xv.y, xv.z, xv.w};
+  const uint32_t h[4] = {hv.x, hv.y, hv.z, hv.w};
+  const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+  uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float y = __uint_as_float(scaled_bf16_fast(fx[i], fw[i], r) << 16);
-    hn[i] = __uint_as_float(residual_bf16_fast(fh[i], y, coef) << 16);
-    acc_add(acc, __fmul_rn(hn[i], hn[i]));
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t yb = scaled_bf16x2_fast(make_float2(bf16_lo(x[i]), bf16_hi(x[i])),
+                                           make_float2(bf16_lo(w[i]), bf16_hi(w[i])), r);
+    o[i] = residual_bf16x2_fast(make_float2(bf16_lo(h[i]), bf16_hi(h[i])), make_float2(bf16_lo(yb), bf16_hi(yb)),
+                                coef);
+    const float2 hn = make_float2(bf16_lo(o[i]), bf16_hi(o[i]));
+    acc_add2(acc, __fmul2_rn(hn, hn));
   }
-  return pack8(hn);
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ uint4 chunk_scale(const uint4& hv, const uint4& wv, const F2& r) {
-  float fh[8], fw[8];
-  unpack8(hv, fh);
-  unpack8(wv, fw);
-  uint32_t o[8];
+  const uint32_t h[4] = {hv.x, hv.y, hv.z, hv.w};
+  const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+  uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = scaled_bf16_fast(fh[i], fw[i], r);
-  return make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16), o[6] | (o[7] << 16));
+  for (int i = 0; i < 4; ++i)
+    o[i] = scaled_bf16x2_fast(make_float2(bf16_lo(h[i]), bf16_hi(h[i])), make_float2(bf16_lo(w[i]), bf16_hi(w[i])),
+                              r);
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // block-wide sum of squares -> 1/sqrt(mean + eps), evaluated by one thread;

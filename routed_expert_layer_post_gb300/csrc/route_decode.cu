@@ -159,12 +159,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const size_t idx = static_cast<size_t>(t) * nc + c;
       const uint4 xv = x[idx];
       const uint4 hv = h[idx];
-      F2 acc{0.f, 0.f};
-      acc_squares(acc, xv);
-      const F2 r = block_rsqrt_mean(acc, red, nwarps, inv_h, eps);
-      F2 acc2{0.f, 0.f};
+      F2x2 acc{{0.f, 0.f}, {0.f, 0.f}};
+      acc_squares2(acc, xv);
+      const F2 r = block_rsqrt_mean(fold(acc), red, nwarps, inv_h, eps);
+      F2x2 acc2{{0.f, 0.f}, {0.f, 0.f}};
       hc[t] = chunk_residual(xv, hv, wp, r, coef, acc2);
-      const F2 r2 = block_rsqrt_mean(acc2, red, nwarps, inv_h, eps);
+      const F2 r2 = block_rsqrt_mean(fold(acc2), red, nwarps, inv_h, eps);
       zc[t] = chunk_scale(hc[t], wq, r2);
       // router logits of the block's experts: z . W_r[e] in fp32 FMA, fixed reduction order
       float zf[8];
