@@ -9,10 +9,13 @@ shapes (hidden 5120, 256 experts in 8 groups, top 4 groups / top 8 experts,
 d_ff 2560, n = 20).
 
 Timing: W untimed warm-up steps, then K steps. Before each step a 512 MB
-buffer is overwritten (L2 is 129 MB) and the input batch rotates over
-``--batches`` seeded draws, so expert weights come from HBM; CUDA events
-recorded by the library at the stage boundaries time each step and each
-kernel on the launching stream. The flush is outside the events.
+buffer is overwritten (L2 is 129 MB) and then read back, so L2 holds none of
+the step's data and no dirty lines whose write-back would fall inside the
+step; the input batch rotates over ``--batches`` seeded draws, so expert
+weights come from HBM. CUDA events recorded by the library at the stage
+boundaries time each step and each kernel on the launching stream. The flush
+is outside the events; ``--l2-flush write`` skips the read-back (both are
+reported).
 
 Prints one JSON line (rank 0). Multi-GPU (torchrun): every rank runs the same
 workload on its own GPU (tokens are independent: replicas, weak scaling); the
@@ -57,6 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--num-experts", type=int, default=None,
                    help="override E (same per-expert shapes; for small-footprint profiling runs)")
     p.add_argument("--tokens", type=int, default=None, help="override T (for small-footprint profiling runs)")
+    p.add_argument("--l2-flush", choices=["write-read", "write"], default="write-read",
+                   help="before every step: overwrite a 512 MB buffer, then (write-read) read it back so the "
+                        "overwrite's dirty lines are written back before the step rather than inside it")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time direct launches only (no CUDA-graph pass)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -348,6 +354,15 @@ def run_ours(args):
     ws_bytes = lib.beam_moe_workspace_size(ctypes.byref(mc), T)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush_words = flush.view(torch.int64)
+
+    def flush_l2(mode=args.l2_flush):
+        # The overwrite (4x L2) evicts every line of the previous step but
+        # leaves L2 full of dirty lines; reading the buffer back writes those
+        # back first, so the step starts from a cold, clean L2.
+        flush.zero_()
+        if mode == "write-read":
+            flush_words.sum()
     stream = torch.cuda.current_stream(device)
     sp = stream.cuda_stream
 
@@ -384,7 +399,7 @@ def run_ours(args):
     # warm-up; also records how many experts each batch touches
     touched = []
     for i in range(max(W, B)):
-        flush.zero_()
+        flush_l2()
         step(i, dbg_plain)
         if i < B:
             touched.append(int((torch.diff(offs) > 0).sum().item()))
@@ -408,14 +423,14 @@ def run_ours(args):
                 raise RuntimeError(f"beam_moe_layer (capture): {beam.beam_status_string(st)}")
             graphs.append(g)
         for i in range(W):
-            flush.zero_()
+            flush_l2()
             graphs[i % B].replay()
         torch.cuda.synchronize()
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
 
-    def replay(i, flush_l2=True):
-        if flush_l2:
-            flush.zero_()
+    def replay(i, flush_mode=args.l2_flush):
+        if flush_mode is not None:
+            flush_l2(flush_mode)
         gev[i][0].record(stream)
         graphs[i % B].replay()
         gev[i][1].record(stream)
@@ -424,22 +439,28 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(gpu_id_for(device.index)) as clocks:
         for i in range(K):
-            flush.zero_()
+            flush_l2()
             step(i, main[i][1])
         torch.cuda.synchronize()
         for i in range(K if graphs else 0):
             replay(i)
         torch.cuda.synchronize()
     graph_ms = [gev[i][0].elapsed_time(gev[i][1]) for i in range(K)] if graphs else []
-    warm_ms = []
+    warm_ms, other_ms = [], []
     if graphs:
         for i in range(min(K, 200)):
-            replay(i, flush_l2=False)
+            replay(i, flush_mode=None)
         torch.cuda.synchronize()
         warm_ms = [gev[i][0].elapsed_time(gev[i][1]) for i in range(min(K, 200))]
+        # the same replays after a write-only flush (L2 left full of dirty lines)
+        other = "write" if args.l2_flush == "write-read" else "write-read"
+        for i in range(min(K, 200)):
+            replay(i, flush_mode=other)
+        torch.cuda.synchronize()
+        other_ms = [gev[i][0].elapsed_time(gev[i][1]) for i in range(min(K, 200))]
     barrier()
     for i in range(K2):
-        flush.zero_()
+        flush_l2()
         step(i, stages[i][1])
     torch.cuda.synchronize()
 
@@ -509,14 +530,20 @@ def run_ours(args):
         ws_h = torch.empty(hbytes, dtype=torch.uint8, device=device)
         ho = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
         yo = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        # a serving loop's staging buffers: each step's batch is written into
+        # the same page-locked h and x (host to host, before the timed call)
+        hi = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        xi = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
         Ke = min(K, 200)
         tot = 0.0
         for i in range(Ke + 3):
-            flush.zero_()
-            torch.cuda.synchronize()
             b = i % B
+            hi.copy_(hs_host[b])
+            xi.copy_(xs_host[b])
+            flush_l2()
+            torch.cuda.synchronize()
             t0 = time.perf_counter()
-            st = lib.beam_moe_layer_host(hs_host[b].data_ptr(), xs_host[b].data_ptr(), cfg.n,
+            st = lib.beam_moe_layer_host(hi.data_ptr(), xi.data_ptr(), cfg.n,
                                          ctypes.byref(weights), T, ctypes.byref(mc), ho.data_ptr(), yo.data_ptr(),
                                          ws_h.data_ptr(), hbytes, sp)
             dt = time.perf_counter() - t0
@@ -526,7 +553,10 @@ def run_ours(args):
                 tot += dt
         tot = reduce_max(tot, device)
         e2e = {"value": T * Ke * world / tot, "unit": UNIT, "h2d_bytes_per_step": 2 * T * H * 2,
-               "d2h_bytes_per_step": 2 * T * H * 2, "steps": Ke}
+               "d2h_bytes_per_step": 2 * T * H * 2, "steps": Ke,
+               "timing": "host clock around beam_moe_layer_host (returns after a stream synchronise); the same "
+                         "page-locked h, x, h', y buffers every step, refilled with the step's batch before the "
+                         "timed call"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -542,7 +572,9 @@ def run_ours(args):
                "dtype": "bf16", "data": "synthetic",
                "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "G": cfg.G, "TG": cfg.TG, "K": cfg.K,
                           "F": F, "n": cfg.n, "parallelism": f"replicas x{world}",
-                          "l2": "512 MB buffer overwritten before every step (outside the timed events); "
+                          "l2": "512 MB buffer overwritten "
+                                + ("and read back " if args.l2_flush == "write-read" else "")
+                                + "before every step (outside the timed events); "
                                 f"inputs rotate over {B} seeded batches",
                           "weights": "expert weights bf16 N(0, 1/sqrt(fan_in)) drawn on the device; router, "
                                      "norms, bias and activations from beam_inputs"},
@@ -552,6 +584,8 @@ def run_ours(args):
                "direct_launch": {"value": direct_value, "unit": UNIT,
                                  "us_per_layer": 1e3 * statistics.fmean(step_ms)},
                "graph_warm_l2_us_per_layer": 1e3 * statistics.fmean(warm_ms) if warm_ms else None,
+               f"graph_{'write_only' if args.l2_flush == 'write-read' else 'write_read'}_flush_us_per_layer":
+                   1e3 * statistics.fmean(other_ms) if other_ms else None,
                "stage_us": stage_report(stage_ms, routing_fused(cfg, T)),
                "us_per_layer_with_stage_events": 1e3 * statistics.fmean(staged_step_ms),
                "touched_experts_mean": statistics.fmean(touched_per_step),

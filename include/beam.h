@@ -207,12 +207,24 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n,
  * from the mapped memory and the layer writes h_out and y_out to it directly
  * instead of four copy-engine transfers; the results are the same bits. h_out
  * must not alias x; y_out must alias none of the others. Weights stay device
- * pointers. Workspace: beam_moe_layer_host_workspace_size. */
+ * pointers. Workspace: beam_moe_layer_host_workspace_size.
+ * Repeated calls on that mapped-memory path: the second call with the same
+ * device, buffers, n, T, weights, config and workspace captures its launches
+ * into a CUDA graph, and later calls with the same arguments replay it (one
+ * launch instead of five; the same kernels and results). The library keeps up
+ * to 256 such graphs per process, evicting the least recently used;
+ * beam_release_host_graphs frees them. Buffer contents may change freely
+ * between calls; the graphs hold only addresses. */
 size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T);
 beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
                                   const beam_moe_weights_t* weights, int T,
                                   const beam_moe_config_t* cfg, uint16_t* h_out_host,
                                   uint16_t* y_out_host, void* ws, size_t ws_bytes, void* stream);
+
+/* Frees every graph that beam_moe_layer_host has captured (their memory
+ * only: a captured graph runs only when a call repeats its exact arguments,
+ * so freeing or reusing buffers needs no release first). Always BEAM_OK. */
+beam_status_t beam_release_host_graphs(void);
 
 /* Reads and clears the library's device error word on the current device
  * after synchronising `stream`. *code receives 0 if no bounded wait timed

@@ -24,7 +24,7 @@ __all__ = [
     "beam_moe_gate_up", "beam_moe_down", "beam_moe_combine", "beam_moe_layer",
     "beam_moe_layer_host", "beam_moe_workspace_size", "beam_moe_permute_workspace_size",
     "beam_moe_experts_workspace_size", "beam_moe_layer_host_workspace_size",
-    "beam_get_device_error", "beam_check_bounded_wait", "beam_last_launch_count", "beam_status_string", "Workspace",
+    "beam_get_device_error", "beam_check_bounded_wait", "beam_release_host_graphs", "beam_last_launch_count", "beam_status_string", "Workspace",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbeam.so")
@@ -87,6 +87,7 @@ _SIGNATURES = {
                                     c_void_p]),
     "beam_get_device_error": (c_int, [ctypes.POINTER(c_int), c_void_p]),
     "beam_check_bounded_wait": (c_int, [c_void_p, c_int, ctypes.POINTER(c_int), c_void_p]),
+    "beam_release_host_graphs": (c_int, []),
     "beam_moe_permute_no_alloc": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeConfig), c_void_p,
                                           c_void_p, c_void_p, c_void_p, c_void_p]),
 }
@@ -319,6 +320,11 @@ def beam_get_device_error() -> int:
     if status not in (0, 6):
         _check("beam_get_device_error", status)
     return code.value
+
+
+def beam_release_host_graphs() -> None:
+    """Frees the CUDA graphs that repeated host-buffer layer calls captured."""
+    _check("beam_release_host_graphs", library().beam_release_host_graphs())
 
 
 def beam_check_bounded_wait(limit_ms: int = 50) -> int:

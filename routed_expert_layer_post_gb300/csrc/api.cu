@@ -4,6 +4,7 @@
 // layer variant and the device-error query).
 #include "../../include/beam.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 #include <algorithm>
 #include <cmath>
@@ -361,9 +362,12 @@ size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int T) {
   return layer_ws(cfg, T, plan_sms()).total;
 }
 
-beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const beam_moe_weights_t* wt, int T,
-                             const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
-                             const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream) {
+// beam_moe_layer; `route_sync_zeroed`: an earlier kernel on the stream zeroed
+// the decode routing kernel's flags (no memset before it).
+static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, const beam_moe_weights_t* wt, int T,
+                                const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
+                                const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream,
+                                bool route_sync_zeroed) {
   beam_status_t st = check_config(cfg);
   if (st != BEAM_OK) return st;
   if ((st = check_T(T, cfg)) != BEAM_OK) return st;
@@ -413,7 +417,7 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
     e = beam::launch_route_decode(h, x, wt->w_post, wt->w_pre, wt->router_w, wt->bias, T, H, cfg->num_experts,
                                   cfg->num_groups, cfg->topk_groups, cfg->topk, cfg->routed_scale, cfg->eps, n,
                                   h_out, z, logits, ids, w, offsets, perm, inv, x_perm, router_ticket, gemm_scratch,
-                                  beam::gemm_clear_bytes(p0, p1), d.sms, s, pdl);
+                                  beam::gemm_clear_bytes(p0, p1), d.sms, s, pdl, route_sync_zeroed);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
     record(dbg, 1, s);
     record(dbg, 2, s);
@@ -460,6 +464,12 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
   return st;
 }
 
+beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const beam_moe_weights_t* wt, int T,
+                             const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
+                             const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream) {
+  return layer_impl(h, x, n, wt, T, cfg, h_out, y_out, dbg, ws, ws_bytes, stream, false);
+}
+
 size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T) {
   const size_t base = beam_moe_workspace_size(cfg, T);
   if (base == 0 && T != 0) return 0;
@@ -480,12 +490,133 @@ void* mapped_host(const void* p) {
 }
 
 // h and x from mapped host memory into the device workspace in one launch.
+// It also zeroes the decode routing kernel's flags (`sync`, may be null), so
+// that kernel needs no memset before it and starts at once: its loads of the
+// router rows and norm weights overlap the reads of host memory here.
 __global__ void stage_in_kernel(const uint4* __restrict__ h, const uint4* __restrict__ x, uint4* __restrict__ dh,
-                                uint4* __restrict__ dx, int n16) {
+                                uint4* __restrict__ dx, int n16, int* __restrict__ sync, int sync_ints) {
+  beam::ptx::griddep_launch_dependents();
+  if (sync != nullptr && blockIdx.x == 0 && static_cast<int>(threadIdx.x) < sync_ints) sync[threadIdx.x] = 0;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x) {
     dh[i] = h[i];
     dx[i] = x[i];
   }
+}
+
+// One zero-copy host call: its device-visible buffers and every argument
+// that enters a kernel. Zero-filled before use, so whole keys compare with
+// memcmp (padding included).
+struct HostCall {
+  int device, n, T;
+  const void* h;
+  const void* x;
+  void* h_out;
+  void* y_out;
+  beam_moe_weights_t wt;
+  beam_moe_config_t cfg;
+  void* ws;
+  size_t ws_bytes;
+};
+
+uint64_t hash_call(const HostCall& k) {  // FNV-1a over the key's bytes
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+  uint64_t v = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof k; ++i) v = (v ^ b[i]) * 1099511628211ull;
+  return v;
+}
+
+// The launches of a zero-copy call: stage-in, then the layer writing h' and y
+// to the mapped output buffers. Sets the thread's launch count.
+beam_status_t zero_copy_launches(const HostCall& k, cudaStream_t s) {
+  const size_t bytes = static_cast<size_t>(k.T) * k.cfg.hidden * 2;
+  const size_t act = align_up(bytes);
+  char* base = static_cast<char*>(k.ws);
+  uint16_t* d_h = reinterpret_cast<uint16_t*>(base);
+  uint16_t* d_x = reinterpret_cast<uint16_t*>(base + act);
+  char* lws = base + 4 * act;
+  const size_t lws_bytes = k.ws_bytes - 4 * act;
+  const bool route = beam::route_decode_supported(k.T, k.cfg.hidden, k.cfg.num_experts, k.cfg.num_groups,
+                                                  k.cfg.topk);
+  int* sync = route ? reinterpret_cast<int*>(lws + layer_ws(&k.cfg, k.T, plan_sms()).router_ticket) : nullptr;
+  const int n16 = static_cast<int>(bytes / 16);
+  stage_in_kernel<<<(n16 + 255) / 256, 256, 0, s>>>(static_cast<const uint4*>(k.h), static_cast<const uint4*>(k.x),
+                                                  reinterpret_cast<uint4*>(d_h), reinterpret_cast<uint4*>(d_x), n16,
+                                                  sync, beam::kRouteSyncInts);
+  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+  const beam_status_t st = layer_impl(d_h, d_x, k.n, &k.wt, k.T, &k.cfg, static_cast<uint16_t*>(k.h_out),
+                                      static_cast<uint16_t*>(k.y_out), nullptr, lws, lws_bytes, s, route);
+  launch_counter() += 1;
+  return st;
+}
+
+// Graphs of repeated zero-copy calls. A decode loop makes the same call (same
+// buffers, weights and workspace) once per token, so the second call with a
+// given key captures its launches into a CUDA graph and later calls replay it
+// with one launch. Keys seen once run as direct launches: a loop over more
+// keys than the table holds never pays for a capture it cannot reuse.
+struct HostGraph {
+  HostCall key;
+  uint64_t hash = 0, last_use = 0;
+  cudaGraphExec_t exec = nullptr;
+  int launches = 0;
+  bool used = false, failed = false;
+};
+
+constexpr int kHostGraphs = 256;
+std::mutex g_graph_mu;
+HostGraph g_graphs[kHostGraphs];
+uint64_t g_graph_tick = 0;
+cudaStream_t g_capture_stream[64] = {};
+
+HostGraph* find_graph(const HostCall& k, uint64_t hash) {
+  for (HostGraph& g : g_graphs)
+    if (g.used && g.hash == hash && std::memcmp(&g.key, &k, sizeof k) == 0) return &g;
+  return nullptr;
+}
+
+HostGraph* insert_graph(const HostCall& k, uint64_t hash) {
+  HostGraph* v = &g_graphs[0];
+  for (HostGraph& g : g_graphs) {
+    if (!g.used) {
+      v = &g;
+      break;
+    }
+    if (g.last_use < v->last_use) v = &g;
+  }
+  if (v->exec != nullptr) cudaGraphExecDestroy(v->exec);  // freed once any replay in flight ends
+  *v = HostGraph{};
+  v->key = k;
+  v->hash = hash;
+  v->used = true;
+  return v;
+}
+
+// Captures the call on a private stream; false (and the table entry marked
+// failed) when any step of the capture fails.
+bool capture_graph(HostGraph* g) {
+  cudaStream_t& cs = g_capture_stream[g->key.device];
+  if (cs == nullptr && cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    cs = nullptr;
+    cudaGetLastError();
+    g->failed = true;
+    return false;
+  }
+  cudaGraph_t graph = nullptr;
+  bool ok = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+  if (ok) {
+    launch_counter() = 0;
+    ok = zero_copy_launches(g->key, cs) == BEAM_OK;
+    g->launches = launch_counter();
+    ok = (cudaStreamEndCapture(cs, &graph) == cudaSuccess) && ok && graph != nullptr;
+  }
+  if (ok) ok = cudaGraphInstantiate(&g->exec, graph, 0) == cudaSuccess;
+  if (graph != nullptr) cudaGraphDestroy(graph);
+  if (!ok) {
+    g->exec = nullptr;
+    g->failed = true;
+    cudaGetLastError();
+  }
+  return ok;
 }
 
 }  // namespace
@@ -520,15 +651,39 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
     void* myo = mapped_host(y_out_host);
     if (mh && mx && mho && myo && aligned16(mh) && aligned16(mx) && aligned16(mho) && aligned16(myo) &&
         mho != mx && myo != mh && myo != mx && myo != mho) {
-      const int n16 = static_cast<int>(bytes / 16);
-      stage_in_kernel<<<(n16 + 255) / 256, 256, 0, s>>>(static_cast<const uint4*>(mh), static_cast<const uint4*>(mx),
-                                                      reinterpret_cast<uint4*>(d_h), reinterpret_cast<uint4*>(d_x),
-                                                      n16);
-      if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
-      st = beam_moe_layer(d_h, d_x, n, wt, T, cfg, static_cast<uint16_t*>(mho), static_cast<uint16_t*>(myo),
-                          nullptr, base + 4 * act, ws_bytes - 4 * act, stream);
-      if (st != BEAM_OK) return st;
-      launch_counter() += 1;
+      HostCall k;
+      std::memset(&k, 0, sizeof k);
+      if (cudaGetDevice(&k.device) != cudaSuccess || k.device < 0 || k.device >= 64) return BEAM_ERR_CUDA;
+      k.n = n;
+      k.T = T;
+      k.h = mh;
+      k.x = mx;
+      k.h_out = mho;
+      k.y_out = myo;
+      k.wt = *wt;
+      k.cfg = *cfg;
+      k.ws = ws;
+      k.ws_bytes = ws_bytes;
+      const uint64_t hash = hash_call(k);
+      bool direct = true;
+      {
+        std::lock_guard<std::mutex> lock(g_graph_mu);
+        HostGraph* g = find_graph(k, hash);
+        if (g == nullptr) {
+          insert_graph(k, hash)->last_use = ++g_graph_tick;
+        } else {
+          g->last_use = ++g_graph_tick;
+          if (g->exec != nullptr || (!g->failed && capture_graph(g))) {
+            if (cudaGraphLaunch(g->exec, s) != cudaSuccess) return BEAM_ERR_CUDA;
+            launch_counter() = g->launches;
+            direct = false;
+          }
+        }
+      }
+      if (direct) {
+        launch_counter() = 0;
+        if ((st = zero_copy_launches(k, s)) != BEAM_OK) return st;
+      }
       return cuda_status(cudaStreamSynchronize(s));
     }
   }
@@ -539,6 +694,16 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
   if (cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaMemcpyAsync(y_out_host, d_y, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
+}
+
+beam_status_t beam_release_host_graphs(void) {
+  std::lock_guard<std::mutex> lock(g_graph_mu);
+  for (HostGraph& g : g_graphs) {
+    if (g.exec != nullptr && cudaGraphExecDestroy(g.exec) != cudaSuccess) cudaGetLastError();
+    g = HostGraph{};
+  }
+  g_graph_tick = 0;
+  return BEAM_OK;
 }
 
 beam_status_t beam_get_device_error(int* code, void* stream) {

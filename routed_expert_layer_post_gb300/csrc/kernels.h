@@ -44,9 +44,10 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 // Boundary -> router -> top-k -> permutation -> row gather in one launch, and
 // `clear_bytes` of `clear` zeroed (the experts' counters and tickets), for
 // T <= 8 with 256 experts in 8 groups. `sync` (kRouteSyncInts ints, zeroed by
-// a memset before the launch): [0] the blocks' ticket (left zero), [1] set
-// once offsets, permutation and the cleared scratch are valid, [2] set once
-// the permuted rows are valid (the fused experts launch polls [1] and [2]).
+// a memset before the launch unless `sync_zeroed`: then an earlier kernel on
+// the stream zeroed them): [0] the blocks' ticket (left zero), [1] set once
+// offsets, permutation and the cleared scratch are valid, [2] set once the
+// permuted rows are valid (the fused experts launch polls [1] and [2]).
 constexpr int kRouteSyncInts = 4;
 bool route_decode_supported(int T, int H, int E, int G, int K);
 cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
@@ -54,7 +55,7 @@ cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint
                                 float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
                                 int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
                                 uint16_t* x_perm, int* sync, void* clear, size_t clear_bytes, int num_sms,
-                                cudaStream_t stream, bool pdl);
+                                cudaStream_t stream, bool pdl, bool sync_zeroed = false);
 
 // ---- permutation (permute.cu)
 size_t permute_scratch_bytes(int T, int K, int E);

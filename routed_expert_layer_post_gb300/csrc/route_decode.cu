@@ -337,9 +337,10 @@ cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint
                                 float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
                                 int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
                                 uint16_t* x_perm, int* sync, void* clear, size_t clear_bytes, int num_sms,
-                                cudaStream_t stream, bool pdl) {
-  cudaError_t err = cudaMemsetAsync(sync, 0, kRouteSyncInts * sizeof(int), stream);
-  if (err != cudaSuccess) return err;
+                                cudaStream_t stream, bool pdl, bool sync_zeroed) {
+  cudaError_t err = cudaSuccess;
+  if (!sync_zeroed && (err = cudaMemsetAsync(sync, 0, kRouteSyncInts * sizeof(int), stream)) != cudaSuccess)
+    return err;
   const ResidualCoef coef = norm::residual_coef(n);
   const F2 inv_h = norm::inv_hidden(H);
   auto kernel = T <= 1 ? route_decode_kernel<1> : T <= 2 ? route_decode_kernel<2>
