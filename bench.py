@@ -458,6 +458,8 @@ def run_ours(args):
             replay(i, flush_mode=other)
         torch.cuda.synchronize()
         other_ms = [gev[i][0].elapsed_time(gev[i][1]) for i in range(min(K, 200))]
+    next_boundary = deferred_combine_report(args, lib, beam, cfg, mc, weights, tens, hs, xs, ws, ws_bytes, B,
+                                            flush_l2, device) if graphs else None
     barrier()
     for i in range(K2):
         flush_l2()
@@ -587,6 +589,7 @@ def run_ours(args):
                f"graph_{'write_only' if args.l2_flush == 'write-read' else 'write_read'}_flush_us_per_layer":
                    1e3 * statistics.fmean(other_ms) if other_ms else None,
                "stage_us": stage_report(stage_ms, routing_fused(cfg, T)),
+               "next_boundary": next_boundary,
                "us_per_layer_with_stage_events": 1e3 * statistics.fmean(staged_step_ms),
                "touched_experts_mean": statistics.fmean(touched_per_step),
                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
@@ -596,6 +599,70 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def deferred_combine_report(args, lib, beam, cfg, mc, weights, tens, hs, xs, ws, ws_bytes, B, flush_l2, device):
+    """Decode sizes: the step followed by the next sublayer's boundary, timed
+    as CUDA-graph replays two ways -- the combine as its own kernel
+    (beam_moe_layer, beam_boundary_norm) and the combine fused into that
+    boundary (beam_moe_layer_uncombined, beam_boundary_norm_combine)."""
+    import torch
+    T, H = cfg.T, cfg.H
+    if T > 64:
+        return None
+    Kr = min(args.steps, 200)
+    h1 = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    h2 = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    z2 = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    wp, wq = tens["w_post"].data_ptr(), tens["w_pre"].data_ptr()
+    n2 = cfg.n + 1
+    gstream = torch.cuda.Stream(device)
+    gs = gstream.cuda_stream
+
+    def separate(b):
+        st = lib.beam_moe_layer(hs[b].data_ptr(), xs[b].data_ptr(), cfg.n, ctypes.byref(weights), T,
+                                ctypes.byref(mc), h1.data_ptr(), y.data_ptr(), None, ws.data_ptr(), ws_bytes, gs)
+        st = st or lib.beam_boundary_norm(h1.data_ptr(), y.data_ptr(), wp, wq, T, H, cfg.eps, n2, h2.data_ptr(),
+                                          z2.data_ptr(), gs)
+        return st
+
+    def fused(b):
+        out = beam.MoeUncombined()
+        st = lib.beam_moe_layer_uncombined(hs[b].data_ptr(), xs[b].data_ptr(), cfg.n, ctypes.byref(weights), T,
+                                           ctypes.byref(mc), h1.data_ptr(), ctypes.byref(out), ws.data_ptr(),
+                                           ws_bytes, gs)
+        st = st or lib.beam_boundary_norm_combine(h1.data_ptr(), out.y_perm, out.topk_w, out.inv_perm, cfg.K, wp,
+                                                  wq, T, H, cfg.eps, n2, h2.data_ptr(), z2.data_ptr(), gs)
+        return st
+
+    res = {}
+    for name, fn in (("separate", separate), ("fused", fused)):
+        graphs = []
+        for b in range(B):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=gstream):
+                st = fn(b)
+            if st != 0:
+                raise RuntimeError(f"{name} next-boundary step: {beam.beam_status_string(st)}")
+            graphs.append(g)
+        stream = torch.cuda.current_stream(device)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kr)]
+        for i in range(3):
+            flush_l2()
+            graphs[i % B].replay()
+        for i in range(Kr):
+            flush_l2()
+            evs[i][0].record(stream)
+            graphs[i % B].replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        res[name] = 1e3 * statistics.fmean(a.elapsed_time(b) for a, b in evs)
+        del graphs
+    return {"separate_us": round(res["separate"], 2), "fused_us": round(res["fused"], 2),
+            "saved_us": round(res["separate"] - res["fused"], 2),
+            "timing": f"{Kr} CUDA-graph replays each after the L2 flush: the step plus the next sublayer's "
+                      "boundary, with the combine as its own kernel or fused into that boundary"}
 
 
 def routing_fused(cfg, T):

@@ -199,6 +199,37 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n,
                              const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
                              const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream);
 
+/* The combine deferred to the next boundary (vLLM Beam summary, kernel
+ * change list: the norm kernel that follows the MoE also combines the top-8
+ * expert outputs). beam_moe_layer_uncombined runs beam_moe_layer up to and
+ * including the down GEMM and leaves out the combine; *out receives the
+ * addresses, inside `ws`, of the combine's inputs, valid until `ws` is next
+ * used. beam_boundary_norm_combine is the next boundary with x taken as that
+ * combine: x[t] = bf16(sum_k topk_w[t][k] * y_perm[inv_perm[t*K+k]]) formed
+ * exactly as beam_moe_combine forms it, then beam_boundary_norm(h, x, ...);
+ * the outputs are the same bits as those two calls, in one launch, and y is
+ * neither written nor read. y_perm bf16 [T*K][H], topk_w fp32 [T][K],
+ * inv_perm int32 [T*K] (-1: dropped pair), K <= 16. h_out may alias h; z_out
+ * aliases nothing; neither may alias y_perm. Both are launched with
+ * programmatic dependent launch: they read their weights (w_post, w_pre;
+ * for the layer also the router and bias) before the previous kernel on the
+ * stream has finished, so no kernel just before them may write those. */
+typedef struct {
+  const uint16_t* y_perm;   /* bf16 [T*K][H]: expert outputs, permuted order */
+  const float* topk_w;      /* fp32 [T][K]: routing weights */
+  const int32_t* inv_perm;  /* int32 [T*K]: row of pair t*K+k in y_perm, -1 if dropped */
+} beam_moe_uncombined_t;
+beam_status_t beam_moe_layer_uncombined(const uint16_t* h, const uint16_t* x, int n,
+                                        const beam_moe_weights_t* weights, int T,
+                                        const beam_moe_config_t* cfg, uint16_t* h_out,
+                                        beam_moe_uncombined_t* out, void* ws, size_t ws_bytes,
+                                        void* stream);
+beam_status_t beam_boundary_norm_combine(const uint16_t* h, const uint16_t* y_perm,
+                                         const float* topk_w, const int32_t* inv_perm, int K,
+                                         const uint16_t* w_post, const uint16_t* w_pre, int T,
+                                         int H, float eps, int n, uint16_t* h_out,
+                                         uint16_t* z_out, void* stream);
+
 /* beam_moe_layer with HOST input and output buffers: copies h and x (host,
  * pinned memory recommended) into the workspace, runs the layer, copies h_out
  * and y_out back to the host buffers, and synchronises the stream before it

@@ -13,6 +13,7 @@ entry point.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 from typing import Optional
 
@@ -22,7 +23,8 @@ __all__ = [
     "BeamError", "MoeConfig", "MoeWeights", "MoeDebug", "make_config", "library",
     "beam_boundary_norm", "beam_router_topk", "beam_moe_permute", "beam_moe_experts",
     "beam_moe_gate_up", "beam_moe_down", "beam_moe_combine", "beam_moe_layer",
-    "beam_moe_layer_host", "beam_moe_workspace_size", "beam_moe_permute_workspace_size",
+    "beam_moe_layer_host", "beam_moe_layer_uncombined", "beam_boundary_norm_combine", "MoeUncombined",
+    "beam_moe_workspace_size", "beam_moe_permute_workspace_size",
     "beam_moe_experts_workspace_size", "beam_moe_layer_host_workspace_size",
     "beam_get_device_error", "beam_check_bounded_wait", "beam_release_host_graphs", "beam_last_launch_count", "beam_status_string", "Workspace",
 ]
@@ -52,6 +54,10 @@ class MoeDebug(ctypes.Structure):
                 ("topk_w", c_void_p), ("expert_offsets", c_void_p), ("stage_events", c_void_p * 7)]
 
 
+class MoeUncombined(ctypes.Structure):
+    _fields_ = [("y_perm", c_void_p), ("topk_w", c_void_p), ("inv_perm", c_void_p)]
+
+
 def make_config(hidden: int, num_experts: int, num_groups: int, topk_groups: int, topk: int,
                 d_ff: int, routed_scale: float = 2.5, eps: float = 1e-6) -> MoeConfig:
     return MoeConfig(hidden, num_experts, num_groups, topk_groups, topk, d_ff, routed_scale, eps)
@@ -78,6 +84,11 @@ _SIGNATURES = {
     "beam_moe_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_int, ctypes.POINTER(MoeConfig), c_void_p,
                                  c_void_p]),
     "beam_moe_workspace_size": (c_size_t, [ctypes.POINTER(MoeConfig), c_int]),
+    "beam_moe_layer_uncombined": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeWeights), c_int,
+                                          ctypes.POINTER(MoeConfig), c_void_p, ctypes.POINTER(MoeUncombined),
+                                          c_void_p, c_size_t, c_void_p]),
+    "beam_boundary_norm_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                           c_int, c_int, c_float, c_int, c_void_p, c_void_p, c_void_p]),
     "beam_moe_layer": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeWeights), c_int,
                                ctypes.POINTER(MoeConfig), c_void_p, c_void_p, ctypes.POINTER(MoeDebug),
                                c_void_p, c_size_t, c_void_p]),
@@ -295,6 +306,48 @@ def beam_moe_layer(h, x, n: int, weights: MoeWeights, cfg: MoeConfig, h_out=None
         _p(h, bf), _p(x, bf), n, ctypes.byref(weights), T, ctypes.byref(cfg), _p(h_out, bf), _p(y_out, bf),
         ctypes.byref(dbg_struct) if dbg_struct is not None else None, buf.data_ptr(), buf.numel(), _stream()))
     return h_out, y_out, dbg
+
+
+def _ws_view(buf: torch.Tensor, ptr: int, dtype, shape):
+    """A tensor over `buf` (a uint8 workspace) starting at device address `ptr`."""
+    off = ptr - buf.data_ptr()
+    nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+    if off < 0 or off + nbytes > buf.numel():
+        raise BeamError("address outside the workspace")
+    return buf[off:off + nbytes].view(dtype).view(*shape)
+
+
+def beam_moe_layer_uncombined(h, x, n: int, weights: MoeWeights, cfg: MoeConfig, h_out=None,
+                              ws: Optional[Workspace] = None):
+    """The layer without its combine. Returns (h_out, (y_perm, topk_w, inv_perm)), the last three
+    views of the workspace (valid until it is next used), ready for beam_boundary_norm_combine."""
+    T = h.shape[0]
+    h_out = torch.empty_like(h) if h_out is None else h_out
+    buf = _ws(beam_moe_workspace_size(cfg, T), ws)
+    out = MoeUncombined()
+    bf = torch.bfloat16
+    _check("beam_moe_layer_uncombined", library().beam_moe_layer_uncombined(
+        _p(h, bf), _p(x, bf), n, ctypes.byref(weights), T, ctypes.byref(cfg), _p(h_out, bf), ctypes.byref(out),
+        buf.data_ptr(), buf.numel(), _stream()))
+    if T == 0:
+        return h_out, None
+    K, H = cfg.topk, cfg.hidden
+    return h_out, (_ws_view(buf, out.y_perm, bf, (T * K, H)), _ws_view(buf, out.topk_w, torch.float32, (T, K)),
+                   _ws_view(buf, out.inv_perm, torch.int32, (T * K,)))
+
+
+def beam_boundary_norm_combine(h, y_perm, topk_w, inv_perm, w_post, w_pre, eps: float, n: int, h_out=None,
+                               z_out=None):
+    """The boundary with x = the combine of (y_perm, topk_w, inv_perm). Returns (h_out, z)."""
+    T, H = h.shape
+    K = topk_w.shape[1] if T > 0 else 1
+    h_out = torch.empty_like(h) if h_out is None else h_out
+    z_out = torch.empty_like(h) if z_out is None else z_out
+    bf = torch.bfloat16
+    _check("beam_boundary_norm_combine", library().beam_boundary_norm_combine(
+        _p(h, bf), _p(y_perm, bf), _p(topk_w, torch.float32), _p(inv_perm, torch.int32), K, _p(w_post, bf),
+        _p(w_pre, bf), T, H, eps, n, _p(h_out, bf), _p(z_out, bf), _stream()))
+    return h_out, z_out
 
 
 def beam_moe_layer_host(h_host: torch.Tensor, x_host: torch.Tensor, n: int, weights: MoeWeights,

@@ -173,7 +173,7 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   }
   record(dbg, 5, s);
-  e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, pdl);
+  if (y != nullptr) e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, pdl);
   record(dbg, 6, s);
   return cuda_status(e);
 }
@@ -363,19 +363,21 @@ size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int T) {
 }
 
 // beam_moe_layer; `route_sync_zeroed`: an earlier kernel on the stream zeroed
-// the decode routing kernel's flags (no memset before it).
+// the decode routing kernel's flags (no memset before it). With `uncombined`
+// (and y_out null) the combine is left out and *uncombined receives the
+// workspace addresses of its inputs.
 static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, const beam_moe_weights_t* wt, int T,
                                 const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
                                 const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream,
-                                bool route_sync_zeroed) {
+                                bool route_sync_zeroed, beam_moe_uncombined_t* uncombined = nullptr) {
   beam_status_t st = check_config(cfg);
   if (st != BEAM_OK) return st;
   if ((st = check_T(T, cfg)) != BEAM_OK) return st;
   if (n < 1 || wt == nullptr) return BEAM_ERR_INVALID_ARG;
   launch_counter() = 0;
   if (T == 0) return BEAM_OK;
-  if (!h || !x || !h_out || !y_out || !ws || !wt->w_post || !wt->w_pre || !wt->router_w || !wt->bias ||
-      !wt->w_gate_up || !wt->w_down)
+  if (!h || !x || !h_out || (y_out == nullptr) == (uncombined == nullptr) || !ws || !wt->w_post || !wt->w_pre ||
+      !wt->router_w || !wt->bias || !wt->w_gate_up || !wt->w_down)
     return BEAM_ERR_INVALID_ARG;
   if (!aligned16(h) || !aligned16(x) || !aligned16(h_out) || !aligned16(y_out) || !aligned16(wt->w_post) ||
       !aligned16(wt->w_pre) || !aligned16(wt->router_w) || !aligned4(wt->bias) || !aligned16(wt->w_gate_up) ||
@@ -399,6 +401,11 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
   int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
   int32_t* inv = reinterpret_cast<int32_t*>(base + L.inv);
   uint16_t* x_perm = reinterpret_cast<uint16_t*>(base + L.x_perm);
+  if (uncombined != nullptr) {
+    uncombined->y_perm = reinterpret_cast<const uint16_t*>(base + L.experts + experts_ws(cfg, T, d.sms).y_perm);
+    uncombined->topk_w = w;
+    uncombined->inv_perm = inv;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int H = cfg->hidden;
   int launches = 0;
@@ -468,6 +475,35 @@ beam_status_t beam_moe_layer(const uint16_t* h, const uint16_t* x, int n, const 
                              const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
                              const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream) {
   return layer_impl(h, x, n, wt, T, cfg, h_out, y_out, dbg, ws, ws_bytes, stream, false);
+}
+
+beam_status_t beam_moe_layer_uncombined(const uint16_t* h, const uint16_t* x, int n, const beam_moe_weights_t* wt,
+                                        int T, const beam_moe_config_t* cfg, uint16_t* h_out,
+                                        beam_moe_uncombined_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (out == nullptr) return BEAM_ERR_INVALID_ARG;
+  *out = beam_moe_uncombined_t{};
+  return layer_impl(h, x, n, wt, T, cfg, h_out, nullptr, nullptr, ws, ws_bytes, stream, false, out);
+}
+
+beam_status_t beam_boundary_norm_combine(const uint16_t* h, const uint16_t* y_perm, const float* topk_w,
+                                         const int32_t* inv_perm, int K, const uint16_t* w_post,
+                                         const uint16_t* w_pre, int T, int H, float eps, int n, uint16_t* h_out,
+                                         uint16_t* z_out, void* stream) {
+  if (T < 0 || n < 1 || K < 1 || !(eps >= 0.0f) || !std::isfinite(eps)) return BEAM_ERR_INVALID_ARG;
+  if (K > 16 || !beam::boundary_supported(H)) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(T) * K >= (1LL << 31)) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  launch_counter() = 0;
+  if (T == 0) return BEAM_OK;
+  if (!h || !y_perm || !topk_w || !inv_perm || !w_post || !w_pre || !h_out || !z_out) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(y_perm) || !aligned16(w_post) || !aligned16(w_pre) || !aligned16(h_out) ||
+      !aligned16(z_out) || !aligned4(topk_w) || !aligned4(inv_perm))
+    return BEAM_ERR_MISALIGNED;
+  if (z_out == h_out || z_out == h || z_out == y_perm || h_out == y_perm) return BEAM_ERR_INVALID_ARG;
+  DeviceInfo d;
+  beam_status_t st = device_info(&d);
+  if (st != BEAM_OK) return st;
+  return cuda_status(beam::launch_boundary_combine(h, y_perm, topk_w, inv_perm, K, w_post, w_pre, T, H, eps, n,
+                                                   h_out, z_out, static_cast<cudaStream_t>(stream), true));
 }
 
 size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T) {

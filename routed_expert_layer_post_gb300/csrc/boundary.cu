@@ -73,9 +73,84 @@ __global__ void __launch_bounds__(1024)
   z_out[idx] = chunk_scale(hn, wq, r2);
 }
 
+// ------------------------------------------------------------------ with the combine fused in
+// The boundary after the MoE sublayer takes as x the weighted sum of the
+// token's K expert outputs (vLLM Beam summary, kernel change list: the norm
+// kernel after the MoE also combines the top-8 outputs). x is formed in
+// registers exactly as the separate combine forms it -- every row requested
+// before the first is used, fp32 FMA in slot order from zero, one bf16
+// rounding -- so the outputs are the bits of combine followed by the
+// boundary, without writing or reading y. KMAX bounds K (register arrays).
+template <int KMAX>
+__global__ void __launch_bounds__(1024)
+    boundary_combine_kernel(const uint4* h, const uint4* __restrict__ y_perm, const float* __restrict__ topk_w,
+                            const int32_t* __restrict__ inv, int K, const uint4* __restrict__ w_post,
+                            const uint4* __restrict__ w_pre, int nc, F2 inv_h, float eps, ResidualCoef coef,
+                            uint4* h_out, uint4* __restrict__ z_out) {
+  __shared__ F2 red[33];
+  const int c = threadIdx.x;  // chunk owned by this thread
+  const int t = blockIdx.x;
+  const int nwarps = blockDim.x >> 5;
+  const uint4 wp = w_post[c];  // weights do not come from the previous kernel
+  const uint4 wq = w_pre[c];
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const size_t idx = static_cast<size_t>(t) * nc + c;
+  const uint4 hv = h[idx];
+  uint4 rows[KMAX];
+  float wk[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    rows[k] = make_uint4(0u, 0u, 0u, 0u);
+    wk[k] = 0.f;
+    if (k < K) {
+      const int p = inv[static_cast<size_t>(t) * K + k];
+      if (p >= 0) {
+        wk[k] = topk_w[static_cast<size_t>(t) * K + k];
+        rows[k] = y_perm[static_cast<size_t>(p) * nc + c];
+      }
+    }
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    if (k < K) {
+      float f[8];
+      unpack8(rows[k], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[k], f[i], acc[i]);
+    }
+  }
+  const uint4 xv = pack8(acc);
+  F2x2 sq{{0.f, 0.f}, {0.f, 0.f}};
+  acc_squares2(sq, xv);
+  const F2 r = block_rsqrt_mean(fold(sq), red, nwarps, inv_h, eps);
+  F2x2 sq2{{0.f, 0.f}, {0.f, 0.f}};
+  const uint4 hn = chunk_residual(xv, hv, wp, r, coef, sq2);
+  h_out[idx] = hn;
+  const F2 r2 = block_rsqrt_mean(fold(sq2), red, nwarps, inv_h, eps);
+  z_out[idx] = chunk_scale(hn, wq, r2);
+}
+
 }  // namespace
 
 bool boundary_supported(int H) { return H > 0 && H % 256 == 0 && H <= 8192; }
+
+cudaError_t launch_boundary_combine(const uint16_t* h, const uint16_t* y_perm, const float* topk_w,
+                                    const int32_t* inv_perm, int K, const uint16_t* w_post, const uint16_t* w_pre,
+                                    int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out,
+                                    cudaStream_t stream, bool pdl) {
+  const ResidualCoef coef = residual_coef(n);
+  const F2 inv_h = inv_hidden(H);
+  auto kernel = K <= 8 ? boundary_combine_kernel<8> : boundary_combine_kernel<16>;
+  const cudaError_t err = launch_kernel(
+      kernel, dim3(T), dim3(H / 8), 0, stream, pdl, reinterpret_cast<const uint4*>(h),
+      reinterpret_cast<const uint4*>(y_perm), topk_w, inv_perm, K, reinterpret_cast<const uint4*>(w_post),
+      reinterpret_cast<const uint4*>(w_pre), H / 8, inv_h, eps, coef, reinterpret_cast<uint4*>(h_out),
+      reinterpret_cast<uint4*>(z_out));
+  ++launch_counter();
+  return err;
+}
 
 cudaError_t launch_boundary(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
                             int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out, cudaStream_t stream,

@@ -21,6 +21,13 @@ cudaError_t launch_boundary(const uint16_t* h, const uint16_t* x, const uint16_t
                             int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out, cudaStream_t stream,
                             bool pdl = false, int* zero_slot = nullptr);
 bool boundary_supported(int H);
+// The boundary with x = the combine of the token's K expert outputs
+// (y_perm rows inv_perm[t*K+k], weights topk_w[t][k]; K <= 16), formed as
+// launch_combine forms it: the same bits as combine followed by the boundary.
+cudaError_t launch_boundary_combine(const uint16_t* h, const uint16_t* y_perm, const float* topk_w,
+                                    const int32_t* inv_perm, int K, const uint16_t* w_post, const uint16_t* w_pre,
+                                    int T, int H, float eps, int n, uint16_t* h_out, uint16_t* z_out,
+                                    cudaStream_t stream, bool pdl = false);
 
 // ---- router (router.cu)
 cudaError_t launch_router_logits(const uint16_t* z, const float* W, int T, int H, int E, float* logits,

@@ -124,3 +124,31 @@ def test_bounded_wait_check_rejects_bad_arguments(beam):
     assert lib.beam_check_bounded_wait(ctypes.c_void_p(256), 0, ctypes.byref(site), None) == 1
     assert lib.beam_check_bounded_wait(ctypes.c_void_p(256), 5000, ctypes.byref(site), None) == 1
     assert lib.beam_check_bounded_wait(ctypes.c_void_p(258), 50, ctypes.byref(site), None) == 1  # misaligned
+
+
+def test_deferred_combine_rejects_bad_arguments(beam):
+    lib = beam.library()
+    c = _cfg(beam)
+    p16 = 0x10000
+    fn = lib.beam_boundary_norm_combine
+    # (h, y_perm, topk_w, inv_perm, K, w_post, w_pre, T, H, eps, n, h_out, z_out, stream)
+    assert fn(None, None, None, None, 8, None, None, 0, 5120, 1e-6, 3, None, None, None) == 0  # empty batch
+    assert fn(p16, p16 + 256, p16, p16, 0, p16, p16, 4, 5120, 1e-6, 3, p16 + 64, p16 + 128, None) == 1  # K = 0
+    assert fn(p16, p16 + 256, p16, p16, 17, p16, p16, 4, 5120, 1e-6, 3, p16 + 64, p16 + 128, None) == 3  # K > 16
+    assert fn(p16, p16 + 256, p16, p16, 8, p16, p16, 4, 5000, 1e-6, 3, p16 + 64, p16 + 128, None) == 3  # H
+    assert fn(p16, p16 + 256, p16, p16, 8, p16, p16, 4, 5120, 1e-6, 0, p16 + 64, p16 + 128, None) == 1  # n
+    assert fn(p16, None, p16, p16, 8, p16, p16, 4, 5120, 1e-6, 3, p16 + 64, p16 + 128, None) == 1  # null y_perm
+    assert fn(p16, p16 + 256, p16 + 2, p16, 8, p16, p16, 4, 5120, 1e-6, 3, p16 + 64, p16 + 128, None) == 2
+    assert fn(p16, p16 + 256, p16, p16, 8, p16, p16, 4, 5120, 1e-6, 3, p16 + 64, p16 + 64, None) == 1  # z on h'
+    assert fn(p16, p16 + 256, p16, p16, 8, p16, p16, 4, 5120, 1e-6, 3, p16 + 256, p16 + 128, None) == 1  # h' on y
+    out = beam.MoeUncombined()
+    w = beam.MoeWeights(p16, p16, p16, p16, p16, p16)
+    lu = lib.beam_moe_layer_uncombined
+    assert lu(p16, p16, 3, ctypes.byref(w), 4, ctypes.byref(c), p16, None, p16, 1 << 40, None) == 1  # no out
+    assert lu(None, None, 3, ctypes.byref(w), 0, ctypes.byref(c), None, ctypes.byref(out), None, 0, None) == 0
+    assert out.y_perm is None and out.topk_w is None and out.inv_perm is None
+    bad = beam.MoeWeights(p16, p16, None, p16, p16, p16)
+    assert lu(p16, p16, 3, ctypes.byref(bad), 4, ctypes.byref(c), p16, ctypes.byref(out), p16, 1 << 40, None) == 1
+    # beam_moe_layer still needs y_out
+    assert lib.beam_moe_layer(p16, p16, 3, ctypes.byref(w), 4, ctypes.byref(c), p16, None, None, p16, 1 << 40,
+                              None) == 1
