@@ -41,7 +41,7 @@ beam_status_t check_config(const beam_moe_config_t* c) {
   if (c->topk_groups > c->num_groups) return BEAM_ERR_INVALID_ARG;
   if (c->topk > c->topk_groups * (c->num_experts / c->num_groups)) return BEAM_ERR_INVALID_ARG;
   if (!beam::boundary_supported(c->hidden)) return BEAM_ERR_UNSUPPORTED_SHAPE;
-  if (c->d_ff % 128 != 0) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  if (c->d_ff % 64 != 0) return BEAM_ERR_UNSUPPORTED_SHAPE;
   if (c->num_experts > 256 || c->num_groups > 32 || c->num_experts / c->num_groups > 32) return BEAM_ERR_UNSUPPORTED_SHAPE;
   if (c->topk > 16) return BEAM_ERR_UNSUPPORTED_SHAPE;
   return BEAM_OK;

@@ -63,7 +63,7 @@ constexpr int kMaxSplit = 20;                   // largest split-K factor (parti
 // One GEMM phase: gate/up (kind 0: two accumulators, SwiGLU epilogue) or
 // down (kind 1: one accumulator).
 struct PhaseParams {
-  CUtensorMap tmap_w;   // weights, 3-D: (k, row, expert)
+  CUtensorMap tmap_w;   // weights, 3-D: (k, row, plane); expert e owns planes e*planes .. +planes-1
   CUtensorMap tmap_x;   // activations, 2-D: (k, permuted row)
   uint16_t* out;
   float* partials;      // split-K partial sums of this phase
@@ -72,7 +72,7 @@ struct PhaseParams {
   int ksteps;           // reduction length / 64
   int split;            // split-K factor
   int out_ld;           // output row length (F for gate/up, H for down)
-  int up_row;           // first up row inside [2F] (gate/up)
+  int planes;           // weight planes per expert: 2 for gate/up (gate rows, up rows), 1 for down
   int max_tiles;        // tiles the workspace was sized for
 };
 
@@ -227,7 +227,7 @@ __device__ __forceinline__ void store_outputs(const PhaseParams& ph, int rows, i
   for (int j = 0; j < 16; ++j) {
     if (c0 + j < valid) {
       const int row = row0 + c0 + j;
-      if (row >= 0 && row < rows) {
+      if (row >= 0 && row < rows && col < ph.out_ld) {
         float val;
         if (kind == 0) {
           const float g = v[0][j];
@@ -510,9 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           if (kps == 2) {
             const bool two = k + 1 < k1;
             ptx::mbar_arrive_expect_tx(&full[stage], (two ? 2u : 1u) * (kTileABytes + C::kTileBBytes));
-            ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e, pol_w);
+            ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e * ph.planes, pol_w);
             if (two)
-              ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], (k + 1) * kBK, w.mb * kBM, w.e, pol_w);
+              ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], (k + 1) * kBK, w.mb * kBM,
+                               w.e * ph.planes, pol_w);
             if (defer) {
               pend_stage[npend] = stage;
               pend_k[npend] = k;
@@ -533,9 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             continue;
           }
           ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
-          ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e, pol_w);
-          if (kind == 0)
-            ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], k * kBK, ph.up_row + w.mb * kBM, w.e,
+          ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e * ph.planes, pol_w);
+          if (kind == 0)  // the up rows: the expert's second plane
+            ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e * ph.planes + 1,
                              pol_w);
           if (dep_ready) {
             ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &ph.tmap_x, &full[stage], k * kBK, row0, pol_x);
@@ -747,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               }
             }
             const int row = row0 + j;
-            if (row >= 0 && row < p.rows) {
+            if (row >= 0 && row < p.rows && col < ph.out_ld) {
               const float val = kind == 0 ? g / (1.0f + __expf(-g)) * u2 : g;
               ph.out[static_cast<size_t>(row) * ph.out_ld + col] = static_cast<uint16_t>(f2bf(val));
             }
@@ -1078,7 +1079,7 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int
   const int bn_max = mode == 0 ? 128 : 256;
   int bn = 16;
   while (bn < bn_max && 1.25 * r > bn) bn <<= 1;
-  const int n_mb = mode == 0 ? F / kBM : H / kBM;
+  const int n_mb = mode == 0 ? (F + kBM - 1) / kBM : H / kBM;
   const int ksteps = mode == 0 ? H / kBK : F / kBK;
   plan.bn = bn;
   plan.max_token_tiles = static_cast<int>(touched + entries / bn);
@@ -1141,12 +1142,16 @@ ScratchLayout scratch_layout(const GemmPlan& g, const GemmPlan& d) {
 bool fill_phase(PhaseParams& ph, int mode, const GemmPlan& plan, const uint16_t* weights, const uint16_t* act_in,
                 int rows, int E, int H, int F, uint16_t* out, char* base, const ScratchLayout& l) {
   const int kdim = mode == 0 ? H : F;  // reduction length
-  const int wrows = mode == 0 ? 2 * F : H;
+  // [E][2F][H] gate/up weights are read as [2E][F][H] (gate rows, then up
+  // rows, of each expert), so a last 128-row block that runs past F reads the
+  // zero fill, not the next rows
+  const int planes = mode == 0 ? 2 : 1;
+  const int prows = mode == 0 ? F : H;  // rows per plane
   {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(wrows),
-                                static_cast<cuuint64_t>(E)};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(prows),
+                                static_cast<cuuint64_t>(E) * planes};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kdim) * 2,
-                                   static_cast<cuuint64_t>(kdim) * 2 * static_cast<cuuint64_t>(wrows)};
+                                   static_cast<cuuint64_t>(kdim) * 2 * static_cast<cuuint64_t>(prows)};
     const cuuint32_t box[3] = {kBK, kBM, 1};
     if (!encode_map(&ph.tmap_w, weights, 3, dims, strides, box)) return false;
   }
@@ -1159,11 +1164,11 @@ bool fill_phase(PhaseParams& ph, int mode, const GemmPlan& plan, const uint16_t*
   ph.out = out;
   ph.tickets = reinterpret_cast<int*>(base + (mode == 0 ? l.tickets0 : l.tickets1));
   ph.partials = plan.split > 1 ? reinterpret_cast<float*>(base + (mode == 0 ? l.partials0 : l.partials1)) : nullptr;
-  ph.n_mb = mode == 0 ? F / kBM : H / kBM;
+  ph.n_mb = (prows + kBM - 1) / kBM;
   ph.ksteps = kdim / kBK;
   ph.split = plan.split;
   ph.out_ld = mode == 0 ? F : H;
-  ph.up_row = F;
+  ph.planes = planes;
   ph.max_tiles = plan.max_tiles;
   return true;
 }
