@@ -63,6 +63,10 @@ def parse_args(argv=None):
     p.add_argument("--l2-flush", choices=["write-read", "write"], default="write-read",
                    help="before every step: overwrite a 512 MB buffer, then (write-read) read it back so the "
                         "overwrite's dirty lines are written back before the step rather than inside it")
+    p.add_argument("--moe-shape", choices=["tp8", "ep8"], default=None,
+                   help="instead of the layer: time the permutation and expert stage at one GPU's share of the "
+                        "layer sharded over 8 GPUs (tp8: 256 experts with d_ff 320; ep8: 32 whole experts, "
+                        "routing over 256), for --tokens tokens (default 1)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time direct launches only (no CUDA-graph pass)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -682,10 +686,109 @@ def stage_report(stage_ms, fused_routing):
     return {s: round(v, 2) for s, v in mean.items()}
 
 
+def run_shard_shape(args):
+    """The permutation and the expert stage (gate/up + SwiGLU, down, combine)
+    at one GPU's share of a Beam layer sharded over eight GPUs, the shapes on
+    which the pages compare MoE kernels: one JSON line, CUDA-graph replays
+    after the L2 flush. Routing is drawn over all 256 experts; under EP8 the
+    permutation drops the pairs of the other GPUs' experts."""
+    import torch
+    import routed_expert_layer_post_gb300 as beam
+    from routed_expert_layer_post_gb300 import build as beam_build
+    from beam_inputs import random_topk_ids
+    beam_build.build()
+    lib = beam.library()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    base = CONFIGS["decode_t1"]
+    T = args.tokens or 1
+    E_route = base.E
+    if args.moe_shape == "tp8":
+        E, F = base.E, base.F // 8
+    else:
+        E, F = base.E // 8, base.F
+    H, K = base.H, base.K
+    mc = beam.make_config(H, E, 8, 4, K, F, base.routed_scale, base.eps)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(2000)
+    w_gu = (torch.randn(E, 2 * F, H, device=device, generator=gen) / H ** 0.5).to(torch.bfloat16)
+    w_d = (torch.randn(E, H, F, device=device, generator=gen) / F ** 0.5).to(torch.bfloat16)
+    B = max(1, args.batches)
+    ids, zs, ws_ = [], [], []
+    for b in range(B):
+        ids.append(torch.from_numpy(random_topk_ids(T, E_route, K, seed=3000 + b).astype(np.int32)).to(device))
+        zs.append((torch.randn(T, H, device=device, generator=gen)).to(torch.bfloat16))
+        w = torch.rand(T, K, device=device, generator=gen) + 0.1
+        ws_.append((base.routed_scale * w / w.sum(dim=1, keepdim=True)).contiguous())
+    rows = T * K
+    offs = torch.empty(E + 1, dtype=torch.int32, device=device)
+    perm = torch.empty(rows, dtype=torch.int32, device=device)
+    inv = torch.empty(rows, dtype=torch.int32, device=device)
+    x_perm = torch.empty(rows, H, dtype=torch.bfloat16, device=device)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    pws = torch.empty(max(256, lib.beam_moe_permute_workspace_size(ctypes.byref(mc), T)), dtype=torch.uint8,
+                      device=device)
+    ews = torch.empty(max(256, lib.beam_moe_experts_workspace_size(ctypes.byref(mc), T)), dtype=torch.uint8,
+                      device=device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    gstream = torch.cuda.Stream(device)
+    gs = gstream.cuda_stream
+    graphs, touched = [], []
+    for b in range(B):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gstream):
+            st = lib.beam_moe_permute(ids[b].data_ptr(), zs[b].data_ptr(), T, ctypes.byref(mc), offs.data_ptr(),
+                                      perm.data_ptr(), inv.data_ptr(), x_perm.data_ptr(), pws.data_ptr(),
+                                      pws.numel(), gs)
+            st = st or lib.beam_moe_experts(x_perm.data_ptr(), offs.data_ptr(), w_gu.data_ptr(), w_d.data_ptr(),
+                                            ws_[b].data_ptr(), inv.data_ptr(), T, ctypes.byref(mc), y.data_ptr(),
+                                            ews.data_ptr(), ews.numel(), gs)
+        if st != 0:
+            raise RuntimeError(f"shard-shape step: {beam.beam_status_string(st)}")
+        graphs.append(g)
+        ib = ids[b].cpu().numpy().reshape(-1)
+        touched.append(len(np.unique(ib[ib < E])))
+    stream = torch.cuda.current_stream(device)
+    Kr = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kr)]
+    words = flush.view(torch.int64)
+    for i in range(args.warmup + Kr):
+        flush.zero_()
+        words.sum()
+        j = i - args.warmup
+        if j >= 0:
+            evs[j][0].record(stream)
+        graphs[i % B].replay()
+        if j >= 0:
+            evs[j][1].record(stream)
+    torch.cuda.synchronize()
+    us = [1e3 * a.elapsed_time(b) for a, b in evs]
+    mean_us = statistics.fmean(us)
+    peaks, peaks_kind = load_peaks()
+    bytes_step = statistics.fmean(touched[i % B] for i in range(Kr)) * 3 * F * H * 2 + 2 * rows * H * 2
+    achieved = bytes_step / (mean_us * 1e-6) / 1e9
+    out = {"metric": f"MoE expert stage at the {args.moe_shape.upper()} per-GPU shape (permutation + gate/up "
+                     "+ down + combine)",
+           "value": T / (mean_us * 1e-6), "unit": UNIT, "us_per_call": mean_us, "n_gpus": 1, "steps": Kr,
+           "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": f"{args.moe_shape}_t{T}", "T": T, "H": H, "E_local": E, "E_routed": E_route,
+                      "K": K, "F": F, "l2": "512 MB buffer overwritten and read back before every call"},
+           "touched_experts_mean": statistics.fmean(touched),
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks_kind,
+                        "algorithmic_bytes": bytes_step,
+                        "note": "weights of the touched local experts plus the token rows in and out; the "
+                                "whole call, so launch and routing-side latency count against it"}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.moe_shape is not None:
+        return run_shard_shape(args)
     return run_ours(args)
 
 

@@ -247,13 +247,29 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
   if (x_perm == nullptr) return;
+  // the block's rows as one flat range of 16-byte chunks over all threads,
+  // four loads in flight per thread before their stores
   const int beg = blockIdx.x * rows_per_block, end = min(total, beg + rows_per_block);
-  for (int i = beg + w; i < end; i += kWarps) {  // one warp per row
-    const int pos = s_pos[i];
-    if (pos < 0) continue;
-    const size_t src = static_cast<size_t>(i / K) * row_chunks;
-    const size_t dst = static_cast<size_t>(pos) * row_chunks;
-    for (int c = lane; c < row_chunks; c += 32) x_perm[dst + c] = z[src + c];
+  const int n = (end - beg) * row_chunks;
+  for (int j0 = tid; j0 < n; j0 += 4 * kThreads) {
+    uint4 v[4];
+    int dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * kThreads;
+      dst[u] = -1;
+      if (j < n) {
+        const int i = beg + j / row_chunks, c = j % row_chunks;
+        const int pos = s_pos[i];
+        if (pos >= 0) {
+          v[u] = z[static_cast<size_t>(i / K) * row_chunks + c];
+          dst[u] = pos * row_chunks + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (dst[u] >= 0) x_perm[dst[u]] = v[u];
   }
 }
 
@@ -270,7 +286,8 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* z, int T, int K, 
                            cudaStream_t stream, bool pdl, void* clear, size_t clear_bytes) {
   const int total = T * K;
   if (total <= kChunk) {
-    const int rows_per_block = 16;
+    // the gather is latency-bound: spread the rows over up to 128 blocks
+    const int rows_per_block = (total + 127) / 128;
     const int blocks = x_perm != nullptr ? (total + rows_per_block - 1) / rows_per_block : 1;
     const cudaError_t err = launch_kernel(
         permute_small_kernel, dim3(blocks), dim3(kThreads), 0, stream, pdl, ids, total, K, E,
