@@ -173,7 +173,9 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   }
   record(dbg, 5, s);
-  if (y != nullptr) e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, pdl);
+  // the combine's predecessor is always the expert launch just above, so it
+  // may start early (it waits for that launch before reading anything)
+  if (y != nullptr) e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, /*pdl=*/true);
   record(dbg, 6, s);
   return cuda_status(e);
 }
