@@ -60,6 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--num-experts", type=int, default=None,
                    help="override E (same per-expert shapes; for small-footprint profiling runs)")
     p.add_argument("--tokens", type=int, default=None, help="override T (for small-footprint profiling runs)")
+    p.add_argument("--d-ff", type=int, default=None,
+                   help="override d_ff (for small-footprint profiling of the kernels that do not depend on it)")
     p.add_argument("--l2-flush", choices=["write-read", "write"], default="write-read",
                    help="before every step: overwrite a 512 MB buffer, then (write-read) read it back so the "
                         "overwrite's dirty lines are written back before the step rather than inside it")
@@ -76,6 +78,8 @@ def parse_args(argv=None):
         CONFIGS[args.config] = CONFIGS[args.config].with_(E=args.num_experts)
     if args.tokens is not None:
         CONFIGS[args.config] = CONFIGS[args.config].with_(T=args.tokens)
+    if args.d_ff is not None:
+        CONFIGS[args.config] = CONFIGS[args.config].with_(F=args.d_ff)
     if args.steps is None:
         args.steps = 500 if CONFIGS[args.config].T <= 64 else 20
     if args.warmup < 3 and args.impl == "ours":
