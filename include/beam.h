@@ -30,7 +30,8 @@
  *   BEAM_OK without launching anything.
  * - Alignment: every bf16 and fp32 tensor must be 16-byte aligned (128-bit
  *   vector loads and TMA); int32 tensors 4-byte aligned.
- * - Supported shapes: H % 256 == 0 and H <= 8192; F % 128 == 0; E <= 256;
+ * - Supported shapes: H % 256 == 0 and H <= 8192; F % 64 == 0 (e.g. 320, one
+ *   GPU's slice of d_ff 2560 under 8-way tensor parallelism); E <= 256;
  *   E % G == 0; G <= 32; E/G <= 32; 1 <= TG <= G; 1 <= K <= 16;
  *   K <= TG * E/G; T * K < 2^31.
  */
