@@ -68,7 +68,7 @@ struct PhaseParams {
   uint16_t* out;
   float* partials;      // split-K partial sums of this phase
   int* tickets;         // split-K tickets of this phase (zero before the launch)
-  int n_mb;             // 128-row weight blocks per plane (the last may run past the plane)
+  int n_mb;             // 128-row weight blocks per expert
   int ksteps;           // reduction length / 64
   int split;            // split-K factor
   int out_ld;           // output row length (F for gate/up, H for down)
