@@ -61,7 +61,10 @@ def test_layer_is_deterministic():
     assert torch.equal(y1, y2) and torch.equal(d1["topk_ids"], d2["topk_ids"])
 
 
-@pytest.mark.parametrize("T", [2, 37, 1000])
+# besides ragged sizes, both sides of every point where the layer changes
+# kernels: one-launch routing (T <= 8), router with fused top-k (T <= 32),
+# tensor-core router (T > 128), one-kernel permutation (T * K <= 2048)
+@pytest.mark.parametrize("T", [2, 8, 9, 32, 33, 37, 128, 129, 256, 257, 1000])
 def test_ragged_batches(T):
     from beam_inputs import make_activations
     m = model("decode_t64")
@@ -69,7 +72,7 @@ def test_ragged_batches(T):
     hb, xb = make_activations(cfg, batch=T)
     h_out, y, dbg = run_layer(m, dev_bf16(hb), dev_bf16(xb))
     from oracle.layer import layer
-    tokens = np.arange(T) if T <= 64 else np.arange(0, T, 16)
+    tokens = np.arange(T) if T <= 64 else np.arange(0, T, 32)
     ref = layer(obf.decode(hb), obf.decode(xb), obf.decode(m.wp_bits), obf.decode(m.wq_bits), m.W_r, m.bias,
                 n=cfg.n, eps=cfg.eps, G=cfg.G, TG=cfg.TG, K=cfg.K, routed_scale=cfg.routed_scale,
                 expert_fn=m.expert_fn_nocache, tokens=tokens, workers=16)
