@@ -86,3 +86,36 @@ def test_host_call_with_in_place_residual_replays():
         torch.cuda.synchronize()
         assert torch.equal(y_buf.view(torch.int16), y_ref.cpu().view(torch.int16)), i
         assert torch.equal(h_buf.view(torch.int16), h_ref.cpu().view(torch.int16)), i
+
+
+def test_more_argument_sets_than_graph_slots():
+    # n is part of an argument set: 100 sets called twice are captured, 300
+    # more then overflow the 256-entry table (evicting the captured graphs),
+    # and the first sets come back; every checked call must give the device
+    # entry point's bits
+    beam = beam_module()
+    m = model("decode_t64")
+    cfg = m.cfg.with_(T=1)
+    beam.beam_release_host_graphs()
+    ws = beam.Workspace()
+    h_in, x_in, h_out, y_out = (torch.empty(1, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(4))
+    hb, xb = make_activations(cfg, batch=760)
+    h_in.copy_(_bf16(hb))
+    x_in.copy_(_bf16(xb))
+
+    def call(n, check):
+        beam.beam_moe_layer_host(h_in, x_in, n, m.weights, m.mc, h_out_host=h_out, y_out_host=y_out, ws=ws)
+        if check:
+            h_dev, y_dev = _device_call(beam, m, hb, xb, n)
+            assert torch.equal(y_out.view(torch.int16), y_dev.view(torch.int16)), n
+            assert torch.equal(h_out.view(torch.int16), h_dev.view(torch.int16)), n
+
+    for rep in range(2):
+        for n in range(2, 102):
+            call(n, check=(rep == 1 and n % 25 == 0))
+    for n in range(102, 402):
+        call(n, check=(n % 100 == 0))
+    for n in range(2, 12):
+        call(n, check=True)
+    assert beam.beam_get_device_error() == 0
+    beam.beam_release_host_graphs()
