@@ -161,3 +161,34 @@ def test_skewed_routing_several_token_tiles_per_expert():
     assert np.all(same | near_tie(ref["route"]))
     mx, rel = layer_errors(f64_of(y)[tokens][same], ref["y"][same])
     assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
+
+
+def test_concurrent_layers_on_two_streams():
+    # two layer calls in flight at once on separate streams and workspaces
+    # share no device state: each gives the bits it gives alone
+    from beam_inputs import make_activations
+    beam = beam_module()
+    m = model("decode_t64")
+    runs = []
+    for T, batch in ((1, 950), (8, 951)):
+        cfg = m.cfg.with_(T=T)
+        hb, xb = make_activations(cfg, batch=batch)
+        runs.append((dev_bf16(hb), dev_bf16(xb)))
+    alone = []
+    for h, x in runs:
+        h_out, y, _ = beam.beam_moe_layer(h, x, m.cfg.n, m.weights, m.mc, ws=beam.Workspace())
+        torch.cuda.synchronize()
+        alone.append((h_out.clone(), y.clone()))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [beam.Workspace(), beam.Workspace()]
+    outs = [None, None]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for i, (h, x) in enumerate(runs):
+            with torch.cuda.stream(streams[i]):
+                outs[i] = beam.beam_moe_layer(h, x, m.cfg.n, m.weights, m.mc, ws=wss[i])
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert torch.equal(outs[i][0].view(torch.int16), alone[i][0].view(torch.int16)), (rep, i)
+            assert torch.equal(outs[i][1].view(torch.int16), alone[i][1].view(torch.int16)), (rep, i)
+    assert beam.beam_get_device_error() == 0
