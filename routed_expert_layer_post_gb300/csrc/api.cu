@@ -657,6 +657,34 @@ bool capture_graph(HostGraph* g) {
   return ok;
 }
 
+// The copy path's side stream and events, one set per device. From
+// kOverlapTokens tokens up, h' (final once the boundary has run) is copied
+// back on the side stream while the rest of the layer computes.
+constexpr int kOverlapTokens = 64;
+
+struct CopyAux {
+  cudaStream_t side = nullptr;
+  cudaEvent_t after_boundary = nullptr, h_copied = nullptr;
+  bool ok = false;
+};
+
+std::mutex g_aux_mu;  // held across a call's use of its device's set
+CopyAux g_aux[64];
+
+CopyAux* copy_aux(int dev) {
+  CopyAux& a = g_aux[dev];
+  if (!a.ok) {
+    if (cudaStreamCreateWithFlags(&a.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.after_boundary, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.h_copied, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    a.ok = true;
+  }
+  return &a;
+}
+
 }  // namespace
 
 beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
@@ -727,6 +755,24 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
   }
   if (cudaMemcpyAsync(d_h, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaMemcpyAsync(d_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  int dev = 0;
+  if (T >= kOverlapTokens && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(g_aux_mu);
+    if (CopyAux* a = copy_aux(dev)) {
+      beam_moe_debug_t dbg;
+      std::memset(&dbg, 0, sizeof dbg);
+      dbg.stage_events[1] = a->after_boundary;  // recorded once h' is written
+      st = layer_impl(d_h, d_x, n, wt, T, cfg, d_hn, d_y, &dbg, base + 4 * act, ws_bytes - 4 * act, stream, false);
+      if (st != BEAM_OK) return st;
+      if (cudaStreamWaitEvent(a->side, a->after_boundary, 0) != cudaSuccess ||
+          cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, a->side) != cudaSuccess ||
+          cudaEventRecord(a->h_copied, a->side) != cudaSuccess ||
+          cudaMemcpyAsync(y_out_host, d_y, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+          cudaStreamWaitEvent(s, a->h_copied, 0) != cudaSuccess)
+        return BEAM_ERR_CUDA;
+      return cuda_status(cudaStreamSynchronize(s));
+    }
+  }
   st = beam_moe_layer(d_h, d_x, n, wt, T, cfg, d_hn, d_y, nullptr, base + 4 * act, ws_bytes - 4 * act, stream);
   if (st != BEAM_OK) return st;
   if (cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
