@@ -4,11 +4,12 @@ import math
 import numpy as np
 import torch
 
-from beam_inputs import CONFIGS, expert_weights, make_activations, make_norm_weights, make_router
+from beam_inputs import (CONFIGS, expert_weights, make_activations, make_all_expert_weights, make_norm_weights,
+                         make_router)
 from oracle import bf16
 from oracle.boundary import boundary
 from oracle.combine import combine
-from oracle.experts import expert_outputs, intermediate, silu, swiglu_ffn
+from oracle.experts import decoded_expert, expert_outputs, intermediate, silu, swiglu_ffn
 from oracle.layer import layer
 from oracle.permute import permute
 
@@ -112,3 +113,22 @@ def test_layer_boundary_and_override():
     np.testing.assert_allclose(same["y"], out["y"], rtol=1e-13, atol=1e-13)
     # the output magnitude is O(1) for unit-variance inputs and 1/sqrt(fan_in) weights
     assert 0.05 < np.sqrt(np.mean(out["y"] ** 2)) < 5
+
+
+def test_decoded_expert_reads_gate_up_and_down_planes():
+    # The packed arrays the C ABI takes (W_gu [E][2F][H]: gate rows, then up
+    # rows; W_down [E][H][F]) are unpacked by the oracle into the same three
+    # matrices the generator draws for each expert, gate and up separately.
+    cfg = CONFIGS["toy"].with_(E=6, G=3, F=64, H=128)
+    W_gu, W_d = make_all_expert_weights(cfg, workers=1, cache=False)
+    for e in (0, 2, 5):
+        g_bits, u_bits, d_bits = expert_weights(cfg, e)
+        Wg, Wu, Wd = decoded_expert(W_gu, W_d, e, cfg.F)
+        assert Wg.shape == (cfg.F, cfg.H) and Wu.shape == (cfg.F, cfg.H) and Wd.shape == (cfg.H, cfg.F)
+        assert np.array_equal(Wg, bf16.decode(g_bits))
+        assert np.array_equal(Wu, bf16.decode(u_bits))
+        assert np.array_equal(Wd, bf16.decode(d_bits))
+        # the three draws differ, so a swapped or shifted plane cannot pass
+        assert not np.array_equal(Wg, Wu)
+    other = decoded_expert(W_gu, W_d, 1, cfg.F)
+    assert not np.array_equal(other[0], bf16.decode(expert_weights(cfg, 0)[0]))

@@ -121,8 +121,15 @@ def test_bias_only_affects_selection():
     bias = np.zeros(16)
     bias[12:16] = 5.0
     r2 = route(logits, bias, 4, 2, 4)
-    assert set(r2["ids"][0].tolist()) >= set()  # runs
     assert 3 in r2["groups"][0].tolist()
+    # every chosen expert lies in a chosen group, and both sets are the
+    # exhaustive search's optimum for these biased scores
+    assert {e // 4 for e in r2["ids"][0].tolist()} <= set(r2["groups"][0].tolist())
+    groups, experts = _brute_force(r2["sb"][0], 4, 2, 4)
+    assert set(r2["groups"][0].tolist()) == groups
+    assert set(r2["ids"][0].tolist()) == experts
+    # the forced group holds the four largest biased scores: all four are taken
+    assert set(r2["ids"][0].tolist()) == {12, 13, 14, 15}
     chosen = r2["ids"][0]
     s2 = 1 / (1 + np.exp(-logits[0, chosen]))
     np.testing.assert_allclose(r2["w"][0], 2.5 * s2 / s2.sum(), rtol=1e-15)
