@@ -40,7 +40,7 @@ from typing import Dict, Optional, Tuple
 import numpy as np
 
 __all__ = [
-    "BeamConfig", "CONFIGS", "make_activations", "make_norm_weights",
+    "BeamConfig", "CONFIGS", "make_activations", "shared_direction", "make_norm_weights",
     "make_router", "expert_weights", "make_all_expert_weights",
     "sample_tokens", "random_topk_ids", "to_bf16_bits", "bits_to_float32",
 ]
@@ -130,14 +130,23 @@ def make_activations(cfg: BeamConfig, T: Optional[int] = None, batch: int = 0) -
     T = cfg.T if T is None else T
     h = _rng(cfg.seed, _S_H, batch).standard_normal((T, cfg.H), dtype=np.float32)
     x = _rng(cfg.seed, _S_X, batch).standard_normal((T, cfg.H), dtype=np.float32)
-    if cfg.activations == "shared_direction":
-        u = _rng(cfg.seed, _S_DIR).standard_normal(cfg.H).astype(np.float64)
-        u = (cfg.shared_norm * u / np.sqrt(np.dot(u, u))).astype(np.float32)
+    u = shared_direction(cfg)
+    if u is not None:
         h += u
         x += u
-    elif cfg.activations != "iid":
-        raise ValueError(cfg.activations)
     return to_bf16_bits(h), to_bf16_bits(x)
+
+
+def shared_direction(cfg: BeamConfig) -> Optional[np.ndarray]:
+    """The vector ``shared_norm * u`` (float32 [H], u a seeded unit vector)
+    that the ``shared_direction`` recipe adds to every row of h and x; None
+    for iid activations."""
+    if cfg.activations == "iid":
+        return None
+    if cfg.activations != "shared_direction":
+        raise ValueError(cfg.activations)
+    u = _rng(cfg.seed, _S_DIR).standard_normal(cfg.H).astype(np.float64)
+    return (cfg.shared_norm * u / np.sqrt(np.dot(u, u))).astype(np.float32)
 
 
 def make_norm_weights(cfg: BeamConfig) -> Tuple[np.ndarray, np.ndarray]:

@@ -153,7 +153,10 @@ beam_status_t beam_moe_permute(const int32_t* topk_ids, const uint16_t* z, int T
  * and E <= 256, else BEAM_ERR_WORKSPACE_TOO_SMALL. All calls on a device share
  * the array: calls whose kernels may overlap on the GPU (unordered streams)
  * race and must not be issued. The first call on each device looks up the
- * array's device address; make it before any stream capture on that device. */
+ * array's device address; make it before any stream capture on that device.
+ * Only a successful lookup is kept (a failed one is retried by the next call),
+ * and it is kept for the life of the process: resetting the device
+ * (cudaDeviceReset) after the first call is not supported. */
 #define BEAM_NO_ALLOC_MAX_PAIRS 131072
 beam_status_t beam_moe_permute_no_alloc(const int32_t* topk_ids, const uint16_t* z, int T,
                                         const beam_moe_config_t* cfg, int32_t* expert_offsets,
@@ -246,7 +249,12 @@ beam_status_t beam_boundary_norm_combine(const uint16_t* h, const uint16_t* y_pe
  * launch instead of five; the same kernels and results). The library keeps up
  * to 256 such graphs per process, evicting the least recently used;
  * beam_release_host_graphs frees them. Buffer contents may change freely
- * between calls; the graphs hold only addresses. */
+ * between calls; the graphs hold only addresses.
+ * After its synchronise the call reads the device error word (see
+ * beam_get_device_error): if a bounded wait inside a kernel gave up, it clears
+ * the word and returns BEAM_ERR_DEVICE_TIMEOUT (the outputs are then
+ * incomplete). The word is shared by every call on the device, so a call may
+ * also report a timeout of another call that overlapped it on the GPU. */
 size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T);
 beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
                                   const beam_moe_weights_t* weights, int T,
@@ -260,7 +268,12 @@ beam_status_t beam_release_host_graphs(void);
 
 /* Reads and clears the library's device error word on the current device
  * after synchronising `stream`. *code receives 0 if no bounded wait timed
- * out, otherwise a nonzero site code; returns BEAM_ERR_DEVICE_TIMEOUT then. */
+ * out, otherwise a nonzero site code; returns BEAM_ERR_DEVICE_TIMEOUT then.
+ * There is one word per device for the whole process: it is not tied to a
+ * stream or a call. A timeout in any call on the device (on any stream) sets
+ * it until some call reads it here, in beam_check_bounded_wait or in
+ * beam_moe_layer_host; callers that run layers on several streams at once
+ * should read it after synchronising all of them. */
 beam_status_t beam_get_device_error(int* code, void* stream);
 
 /* Diagnostic with no counterpart in the pages: checks on the device that a
@@ -273,6 +286,12 @@ beam_status_t beam_get_device_error(int* code, void* stream);
  * site code (*site receives it), BEAM_ERR_DEVICE_TIMEOUT if another site code
  * was pending or none was recorded, BEAM_ERR_INVALID_ARG on bad arguments. */
 beam_status_t beam_check_bounded_wait(int* flag, int limit_ms, int* site, void* stream);
+
+/* The same diagnostic wait, but the site code it records is left pending in
+ * the device error word (for a later beam_get_device_error or
+ * beam_moe_layer_host to report and clear). Synchronises `stream`. Returns
+ * BEAM_OK once the wait has given up, BEAM_ERR_INVALID_ARG on bad arguments. */
+beam_status_t beam_check_bounded_wait_pending(int* flag, int limit_ms, void* stream);
 
 /* Kernel launches issued by the most recent call of each kind on this host
  * thread's view (a count, for reporting). */

@@ -26,7 +26,8 @@ __all__ = [
     "beam_moe_layer_host", "beam_moe_layer_uncombined", "beam_boundary_norm_combine", "MoeUncombined",
     "beam_moe_workspace_size", "beam_moe_permute_workspace_size",
     "beam_moe_experts_workspace_size", "beam_moe_layer_host_workspace_size",
-    "beam_get_device_error", "beam_check_bounded_wait", "beam_release_host_graphs", "beam_last_launch_count", "beam_status_string", "Workspace",
+    "beam_get_device_error", "beam_check_bounded_wait", "beam_check_bounded_wait_pending",
+    "beam_release_host_graphs", "beam_last_launch_count", "beam_status_string", "Workspace",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbeam.so")
@@ -98,6 +99,7 @@ _SIGNATURES = {
                                     c_void_p]),
     "beam_get_device_error": (c_int, [ctypes.POINTER(c_int), c_void_p]),
     "beam_check_bounded_wait": (c_int, [c_void_p, c_int, ctypes.POINTER(c_int), c_void_p]),
+    "beam_check_bounded_wait_pending": (c_int, [c_void_p, c_int, c_void_p]),
     "beam_release_host_graphs": (c_int, []),
     "beam_moe_permute_no_alloc": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeConfig), c_void_p,
                                           c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -388,3 +390,12 @@ def beam_check_bounded_wait(limit_ms: int = 50) -> int:
     _check("beam_check_bounded_wait", library().beam_check_bounded_wait(flag.data_ptr(), limit_ms,
                                                                       ctypes.byref(site), _stream()))
     return site.value
+
+
+def beam_check_bounded_wait_pending(limit_ms: int = 50) -> None:
+    """Runs the device bounded-wait check and leaves its site code pending in
+    the device error word (for the next error query or host-buffer layer call
+    to report)."""
+    flag = torch.zeros(4, dtype=torch.int32, device="cuda")
+    _check("beam_check_bounded_wait_pending",
+           library().beam_check_bounded_wait_pending(flag.data_ptr(), limit_ms, _stream()))

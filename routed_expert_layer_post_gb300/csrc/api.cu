@@ -145,7 +145,7 @@ void record(const beam_moe_debug_t* dbg, int i, cudaStream_t s) {
 beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gu, const uint16_t* w_d,
                           const float* topk_w, const int32_t* inv, int T, const beam_moe_config_t* c, uint16_t* y,
                           char* ws, int sms, cudaStream_t s, const beam_moe_debug_t* dbg = nullptr, bool pdl = false,
-                          bool cleared = false, const int* ready = nullptr) {
+                          bool cleared = false, const int* ready = nullptr, int* err_out = nullptr) {
   const ExpertsWs w = experts_ws(c, T, sms);
   const int rows = T * c->topk;
   uint16_t* act = reinterpret_cast<uint16_t*>(ws + w.act);
@@ -175,7 +175,8 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
   record(dbg, 5, s);
   // the combine's predecessor is always the expert launch just above, so it
   // may start early (it waits for that launch before reading anything)
-  if (y != nullptr) e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, /*pdl=*/true);
+  if (y != nullptr)
+    e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, /*pdl=*/true, err_out);
   record(dbg, 6, s);
   return cuda_status(e);
 }
@@ -367,11 +368,13 @@ size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int T) {
 // beam_moe_layer; `route_sync_zeroed`: an earlier kernel on the stream zeroed
 // the decode routing kernel's flags (no memset before it). With `uncombined`
 // (and y_out null) the combine is left out and *uncombined receives the
-// workspace addresses of its inputs.
+// workspace addresses of its inputs. `err_out` (optional, device-visible):
+// the combine copies the device error word there.
 static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, const beam_moe_weights_t* wt, int T,
                                 const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
                                 const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream,
-                                bool route_sync_zeroed, beam_moe_uncombined_t* uncombined = nullptr) {
+                                bool route_sync_zeroed, beam_moe_uncombined_t* uncombined = nullptr,
+                                int* err_out = nullptr) {
   beam_status_t st = check_config(cfg);
   if (st != BEAM_OK) return st;
   if ((st = check_T(T, cfg)) != BEAM_OK) return st;
@@ -434,7 +437,7 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
     launch_counter() = 0;
     const int* ready = beam::fused_experts_supported(p0, p1) ? router_ticket + 1 : nullptr;
     st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
-                     dbg, pdl, /*cleared=*/true, ready);
+                     dbg, pdl, /*cleared=*/true, ready, err_out);
     launch_counter() += launches;
     return st;
   }
@@ -468,7 +471,7 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
   launches += launch_counter();
   launch_counter() = 0;
   st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
-                   dbg, pdl, /*cleared=*/true);
+                   dbg, pdl, /*cleared=*/true, nullptr, err_out);
   launch_counter() += launches;
   return st;
 }
@@ -541,6 +544,37 @@ __global__ void stage_in_kernel(const uint4* __restrict__ h, const uint4* __rest
   }
 }
 
+// The device error word as seen by the host entry point. The layer's combine
+// kernel copies the word into a page-locked host slot (one per device), so
+// after its stream synchronise the call reads it with a plain load instead of
+// a device-to-host copy. The slot is registered with the driver once per
+// process; if that fails the call reads the word with a copy instead.
+alignas(4096) int g_err_slots[64 * 16];  // one 64-byte slot per device
+std::once_flag g_err_once;
+int* g_err_slots_dev = nullptr;
+
+int* host_error_slot_dev(int dev) {
+  std::call_once(g_err_once, [] {
+    void* d = nullptr;
+    if (cudaHostRegister(g_err_slots, sizeof g_err_slots, cudaHostRegisterMapped | cudaHostRegisterPortable) ==
+            cudaSuccess &&
+        cudaHostGetDevicePointer(&d, g_err_slots, 0) == cudaSuccess)
+      g_err_slots_dev = static_cast<int*>(d);
+    else
+      cudaGetLastError();
+  });
+  return g_err_slots_dev != nullptr ? g_err_slots_dev + 16 * dev : nullptr;
+}
+
+// After the call's stream synchronise: BEAM_ERR_DEVICE_TIMEOUT (and the
+// device word cleared) if a bounded wait on the device gave up.
+beam_status_t host_call_error(int dev, bool slot_used, cudaStream_t s) {
+  if (slot_used && *reinterpret_cast<volatile int*>(&g_err_slots[16 * dev]) == 0) return BEAM_OK;
+  int code = 0;
+  if (beam::read_and_clear_device_error(&code, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  return code != 0 ? BEAM_ERR_DEVICE_TIMEOUT : BEAM_OK;
+}
+
 // One zero-copy host call: its device-visible buffers and every argument
 // that enters a kernel. Zero-filled before use, so whole keys compare with
 // memcmp (padding included).
@@ -554,6 +588,7 @@ struct HostCall {
   beam_moe_config_t cfg;
   void* ws;
   size_t ws_bytes;
+  int* err_out;
 };
 
 uint64_t hash_call(const HostCall& k) {  // FNV-1a over the key's bytes
@@ -582,7 +617,8 @@ beam_status_t zero_copy_launches(const HostCall& k, cudaStream_t s) {
                                                   sync, beam::kRouteSyncInts);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
   const beam_status_t st = layer_impl(d_h, d_x, k.n, &k.wt, k.T, &k.cfg, static_cast<uint16_t*>(k.h_out),
-                                      static_cast<uint16_t*>(k.y_out), nullptr, lws, lws_bytes, s, route);
+                                      static_cast<uint16_t*>(k.y_out), nullptr, lws, lws_bytes, s, route, nullptr,
+                                      k.err_out);
   launch_counter() += 1;
   return st;
 }
@@ -707,6 +743,9 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
   uint16_t* d_hn = reinterpret_cast<uint16_t*>(base + 2 * act);
   uint16_t* d_y = reinterpret_cast<uint16_t*>(base + 3 * act);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BEAM_ERR_CUDA;
+  int* err_slot = host_error_slot_dev(dev);
   // Decode sizes with page-locked buffers: one kernel reads h and x from the
   // mapped host memory and the layer writes h' and y straight to the host
   // buffers, instead of four copy-engine transfers (about 18 us at 1 token).
@@ -719,7 +758,7 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
         mho != mx && myo != mh && myo != mx && myo != mho) {
       HostCall k;
       std::memset(&k, 0, sizeof k);
-      if (cudaGetDevice(&k.device) != cudaSuccess || k.device < 0 || k.device >= 64) return BEAM_ERR_CUDA;
+      k.device = dev;
       k.n = n;
       k.T = T;
       k.h = mh;
@@ -730,6 +769,7 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
       k.cfg = *cfg;
       k.ws = ws;
       k.ws_bytes = ws_bytes;
+      k.err_out = err_slot;
       const uint64_t hash = hash_call(k);
       bool direct = true;
       {
@@ -750,19 +790,20 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
         launch_counter() = 0;
         if ((st = zero_copy_launches(k, s)) != BEAM_OK) return st;
       }
-      return cuda_status(cudaStreamSynchronize(s));
+      if (cudaStreamSynchronize(s) != cudaSuccess) return BEAM_ERR_CUDA;
+      return host_call_error(dev, err_slot != nullptr, s);
     }
   }
   if (cudaMemcpyAsync(d_h, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaMemcpyAsync(d_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
-  int dev = 0;
-  if (T >= kOverlapTokens && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+  if (T >= kOverlapTokens) {
     std::lock_guard<std::mutex> lock(g_aux_mu);
     if (CopyAux* a = copy_aux(dev)) {
       beam_moe_debug_t dbg;
       std::memset(&dbg, 0, sizeof dbg);
       dbg.stage_events[1] = a->after_boundary;  // recorded once h' is written
-      st = layer_impl(d_h, d_x, n, wt, T, cfg, d_hn, d_y, &dbg, base + 4 * act, ws_bytes - 4 * act, stream, false);
+      st = layer_impl(d_h, d_x, n, wt, T, cfg, d_hn, d_y, &dbg, base + 4 * act, ws_bytes - 4 * act, stream, false,
+                      nullptr, err_slot);
       if (st != BEAM_OK) return st;
       if (cudaStreamWaitEvent(a->side, a->after_boundary, 0) != cudaSuccess ||
           cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, a->side) != cudaSuccess ||
@@ -770,14 +811,17 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
           cudaMemcpyAsync(y_out_host, d_y, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
           cudaStreamWaitEvent(s, a->h_copied, 0) != cudaSuccess)
         return BEAM_ERR_CUDA;
-      return cuda_status(cudaStreamSynchronize(s));
+      if (cudaStreamSynchronize(s) != cudaSuccess) return BEAM_ERR_CUDA;
+      return host_call_error(dev, err_slot != nullptr, s);
     }
   }
-  st = beam_moe_layer(d_h, d_x, n, wt, T, cfg, d_hn, d_y, nullptr, base + 4 * act, ws_bytes - 4 * act, stream);
+  st = layer_impl(d_h, d_x, n, wt, T, cfg, d_hn, d_y, nullptr, base + 4 * act, ws_bytes - 4 * act, stream, false,
+                  nullptr, err_slot);
   if (st != BEAM_OK) return st;
   if (cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaMemcpyAsync(y_out_host, d_y, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
-  return cuda_status(cudaStreamSynchronize(s));
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BEAM_ERR_CUDA;
+  return host_call_error(dev, err_slot != nullptr, s);
 }
 
 beam_status_t beam_release_host_graphs(void) {
@@ -795,6 +839,19 @@ beam_status_t beam_get_device_error(int* code, void* stream) {
   *code = 0;
   if (beam::read_and_clear_device_error(code, static_cast<cudaStream_t>(stream)) != cudaSuccess) return BEAM_ERR_CUDA;
   return *code != 0 ? BEAM_ERR_DEVICE_TIMEOUT : BEAM_OK;
+}
+
+beam_status_t beam_check_bounded_wait_pending(int* flag, int limit_ms, void* stream) {
+  if (flag == nullptr || limit_ms < 1 || limit_ms > 1000 || !aligned4(flag)) return BEAM_ERR_INVALID_ARG;
+  DeviceInfo d;
+  beam_status_t st = device_info(&d);
+  if (st != BEAM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  launch_counter() = 0;
+  if (beam::launch_bounded_wait_probe(flag, static_cast<uint64_t>(limit_ms) * 1000000ull, beam::kProbeSite, s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(s));
 }
 
 beam_status_t beam_check_bounded_wait(int* flag, int limit_ms, int* site, void* stream) {

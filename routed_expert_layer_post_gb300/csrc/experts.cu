@@ -18,8 +18,8 @@
 // padding M with absent tokens. Accumulators live in tensor memory (TMEM),
 // double-buffered so the epilogue of one tile overlaps the MMAs of the next.
 //
-// A persistent CTA per SM walks work units u = blockIdx.x + i * gridDim.x.
-// A unit is (expert, row block, token tile, k-split). Experts' row counts are
+// A persistent CTA per SM takes work units from a global counter. A unit is
+// (expert, row block, token tile, k-split). Experts' row counts are
 // read from expert_offsets on the device; the host never synchronises. When
 // there are too few tiles to fill the GPU (decode), the reduction dimension
 // is split; partial sums go to the workspace and the last unit of a tile to
@@ -300,14 +300,30 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   // written before its predecessor started, so it builds its tile table and
   // streams weight tiles now; only its activation loads and its epilogue wait
   // for the gate/up GEMM.
+  // Every unit, the first included, comes from the launch's unit counter, so
+  // unit ids are handed out in increasing order to CTAs that are running.
+  // A down unit waits only on gate/up units (lower ids), which running CTAs
+  // hold and complete without waiting on later units: the launch progresses
+  // however many of its CTAs are resident (another kernel may hold SMs).
+  // Thread 0 (the producer) requests its first id as soon as the counter is
+  // known to be zeroed; the round trip overlaps the tile-table set-up.
+  int u_first = 0;
   if (MODE != 1) {
     if (MODE == 2 && p.ready != nullptr) {
-      if (tid == 0 && !wait_counter(p.ready, 1, abort_flag, 9)) s_flags[2] = 1;
+      if (tid == 0) {
+        if (!wait_counter(p.ready, 1, abort_flag, 9)) s_flags[2] = 1;
+        else u_first = atomicAdd(p.counter, 1);
+      }
       __syncthreads();  // thread 0's acquire orders the offset and counter reads below
     } else {
       ptx::griddep_wait();
+      if (tid == 0) u_first = atomicAdd(p.counter, 1);
     }
     ptx::griddep_launch_dependents();
+  } else if (tid == 0) {
+    // the down GEMM's counter was zeroed two kernels back (the permutation),
+    // which completed before the gate/up GEMM let this launch start
+    u_first = atomicAdd(p.counter, 1);
   }
   for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
   __syncthreads();
@@ -378,11 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler + TMA producer
-    // Units are handed out dynamically: the first one is blockIdx.x, the
-    // rest come from a global counter (the next id is requested while the
-    // current unit's loads are issued), so SMs that stream faster take more
-    // units and all SMs finish together. Each unit id is published to the
-    // MMA and epilogue warps through a small queue in shared memory.
+    // Units are handed out dynamically from a global counter (the next id
+    // is requested while the current unit's loads are issued), so SMs that
+    // stream faster take more units and all SMs finish together. Each unit
+    // id is published to the MMA and epilogue warps through a small queue in
+    // shared memory.
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
       const uint64_t pol_x = ptx::policy_evict_last();   // activation tiles are re-read per row block
@@ -431,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         ready_gtt = pend_gtt;
         return true;
       };
-      int u_next = static_cast<int>(blockIdx.x);
+      int u_next = u_first;
       for (int seq = 0;; ++seq) {
         int u = u_next;
         if (u >= n_units || !ok) u = -1;
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           break;
         }
         // ask for the following unit now: the atomic's round trip overlaps this unit's loads
-        u_next = static_cast<int>(gridDim.x) + atomicAdd(p.counter, 1);
+        u_next = atomicAdd(p.counter, 1);
         const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
@@ -789,12 +805,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 // for four blocks per SM (the kernel is latency-bound on the row loads).
 constexpr int kMaxTopK = 16;
 
+// `err_out` (optional): one thread copies the device error word there once
+// the expert launch before it has completed, so a host caller can read it
+// from page-locked memory without a separate copy.
 template <int KMAX>
 __global__ void __launch_bounds__(256)
     combine_kernel(const uint4* __restrict__ y_perm, const float* __restrict__ w, const int32_t* __restrict__ inv,
-                   int T, int K, int chunks, uint4* __restrict__ y) {
+                   int T, int K, int chunks, uint4* __restrict__ y, int* err_out) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
+  if (err_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *reinterpret_cast<volatile int*>(err_out) = *reinterpret_cast<volatile int*>(&g_device_error);
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<size_t>(T) * chunks) return;
   const int t = static_cast<int>(idx / chunks);
@@ -1252,14 +1273,14 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
 }
 
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,
-                           uint16_t* y, cudaStream_t stream, bool pdl) {
+                           uint16_t* y, cudaStream_t stream, bool pdl, int* err_out) {
   const int chunks = H / 8;
   const size_t n = static_cast<size_t>(T) * chunks;
   const int blocks = static_cast<int>((n + 255) / 256);
   const cudaError_t err = launch_kernel(K <= 8 ? combine_kernel<8> : combine_kernel<kMaxTopK>, dim3(blocks),
                                         dim3(256), 0, stream, pdl,
                                         reinterpret_cast<const uint4*>(y_perm), w, inv_perm, T, K, chunks,
-                                        reinterpret_cast<uint4*>(y));
+                                        reinterpret_cast<uint4*>(y), err_out);
   ++launch_counter();
   return err;
 }

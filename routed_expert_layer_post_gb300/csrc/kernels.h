@@ -103,8 +103,10 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl = false);
+// `err_out` (optional, device-visible): receives the device error word once
+// the expert launch before the combine has completed.
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,
-                           uint16_t* y, cudaStream_t stream, bool pdl = false);
+                           uint16_t* y, cudaStream_t stream, bool pdl = false, int* err_out = nullptr);
 cudaError_t read_and_clear_device_error(int* code, cudaStream_t stream);
 // One bounded wait on `flag` (zeroed here) that nothing sets: records `site`.
 constexpr int kProbeSite = 99;

@@ -22,7 +22,12 @@
 //   without ordering between them) race on it and give wrong results;
 // - the first call on each device looks up the array's device address with
 //   cudaGetSymbolAddress (with that device current); make that first call
-//   before starting any stream capture on the device.
+//   before starting any stream capture on the device. Only a successful
+//   lookup is kept: after a failed one (for example a call made before the
+//   device's context could be created) the next call looks it up again;
+// - the address is kept for the life of the process, so resetting the
+//   device (cudaDeviceReset) after the first call is not supported: the
+//   array may then sit at another address.
 #include "../../include/beam.h"
 #include "kernels.h"
 
@@ -40,20 +45,23 @@ static __device__ __align__(256) int g_permute_scratch[kScratchInts];
 
 constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices] = {};
-cudaError_t g_scratch_err[kMaxDevices] = {};
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mu[kMaxDevices];
 
-// Device address of g_permute_scratch on the current device (looked up once per device).
+// Device address of g_permute_scratch on the current device. A successful
+// lookup is kept per device; a failed one is retried on the next call.
 beam_status_t scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BEAM_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return BEAM_ERR_UNSUPPORTED_DEVICE;
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mu[dev]);
+  if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_permute_scratch);
-    g_scratch_ptr[dev] = (g_scratch_err[dev] == cudaSuccess) ? p : nullptr;
-  });
-  if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return BEAM_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // leave no sticky error from the failed lookup
+      return BEAM_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
   *out = g_scratch_ptr[dev];
   return BEAM_OK;
 }

@@ -124,6 +124,11 @@ def test_bounded_wait_check_rejects_bad_arguments(beam):
     assert lib.beam_check_bounded_wait(ctypes.c_void_p(256), 0, ctypes.byref(site), None) == 1
     assert lib.beam_check_bounded_wait(ctypes.c_void_p(256), 5000, ctypes.byref(site), None) == 1
     assert lib.beam_check_bounded_wait(ctypes.c_void_p(258), 50, ctypes.byref(site), None) == 1  # misaligned
+    pend = lib.beam_check_bounded_wait_pending
+    assert pend(None, 50, None) == 1
+    assert pend(ctypes.c_void_p(256), 0, None) == 1
+    assert pend(ctypes.c_void_p(256), 5000, None) == 1
+    assert pend(ctypes.c_void_p(258), 50, None) == 1
 
 
 def test_deferred_combine_rejects_bad_arguments(beam):

@@ -193,3 +193,42 @@ def test_concurrent_layers_on_two_streams():
             assert torch.equal(outs[i][0].view(torch.int16), alone[i][0].view(torch.int16)), (rep, i)
             assert torch.equal(outs[i][1].view(torch.int16), alone[i][1].view(torch.int16)), (rep, i)
     assert beam.beam_get_device_error() == 0
+
+
+@pytest.mark.parametrize("first", [0, 1])
+def test_concurrent_prefill_and_decode_layers(first):
+    # A 256-token layer (the fused expert launch with one CTA per SM, whose
+    # down units wait on gate/up units of other CTAs) and a one-token layer
+    # in flight at once on two streams, launched in both orders, 20 times:
+    # each call gives the bits it gives alone, and no bounded wait gives up
+    # (the expert launch hands out its units from a counter, so its progress
+    # does not depend on all of its CTAs being resident).
+    from beam_inputs import make_activations
+    beam = beam_module()
+    m = model("decode_t64")
+    runs = []
+    for T, batch in ((256, 960), (1, 961)):
+        cfg = m.cfg.with_(T=T)
+        hb, xb = make_activations(cfg, batch=batch)
+        runs.append((dev_bf16(hb), dev_bf16(xb)))
+    alone = []
+    for h, x in runs:
+        h_out, y, _ = beam.beam_moe_layer(h, x, m.cfg.n, m.weights, m.mc, ws=beam.Workspace())
+        torch.cuda.synchronize()
+        alone.append((h_out.clone(), y.clone()))
+    assert beam.beam_get_device_error() == 0
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [beam.Workspace(), beam.Workspace()]
+    order = [first, 1 - first]
+    torch.cuda.synchronize()
+    for rep in range(20):
+        outs = [None, None]
+        for i in order:
+            h, x = runs[i]
+            with torch.cuda.stream(streams[i]):
+                outs[i] = beam.beam_moe_layer(h, x, m.cfg.n, m.weights, m.mc, ws=wss[i])
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert torch.equal(outs[i][0].view(torch.int16), alone[i][0].view(torch.int16)), (rep, i)
+            assert torch.equal(outs[i][1].view(torch.int16), alone[i][1].view(torch.int16)), (rep, i)
+    assert beam.beam_get_device_error() == 0
