@@ -60,7 +60,61 @@ def test_clock_summary_parsing():
 
 def test_defaults_and_peaks():
     a = bench.parse_args([])
-    assert a.config == "decode_t1" and a.warmup >= 3 and a.steps > 0 and a.impl == "ours"
+    assert a.config == "all" and a.warmup >= 3 and a.impl == "ours"
+    names, head = bench.workloads(a)
+    assert names == ["toy", "decode_t1", "decode_t64", "prefill_t2048", "prefill_t16384"]
+    assert head == "prefill_t16384"
+    assert all(bench.steps_for(a, n) > 0 and bench.batches_for(a, n) > 0 for n in names)
+    one = bench.parse_args(["--config", "decode_t1", "--steps", "7"])
+    assert bench.workloads(one) == (["decode_t1"], "decode_t1") and bench.steps_for(one, "decode_t1") == 7
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--tokens", "8"])  # overrides need a single workload
     peaks, kind = bench.load_peaks()
     assert peaks["hbm_gbs"] > 1000 and kind in ("measured", "fallback")
     assert bench.whole_job(8, 1, [0.5]) == (16.0, 0.5)
+
+
+def _toy_capture():
+    """A capture of the toy workload whose 'GPU' outputs are the oracle's own
+    (to test the parity report's bookkeeping on CPU)."""
+    import numpy as np
+    from beam_inputs import CONFIGS, make_activations, make_all_expert_weights, make_norm_weights, make_router
+    from oracle import bf16 as obf
+    from oracle.experts import decoded_expert
+    from oracle.layer import layer
+    cfg = CONFIGS["toy"]
+    h, x = make_activations(cfg)
+    wp, wq = make_norm_weights(cfg)
+    W_r, bias = make_router(cfg)
+    W_gu, W_d = make_all_expert_weights(cfg, workers=1, cache=False)
+    ref = layer(obf.decode(h), obf.decode(x), obf.decode(wp), obf.decode(wq), W_r, bias, n=cfg.n, eps=cfg.eps,
+                G=cfg.G, TG=cfg.TG, K=cfg.K, routed_scale=cfg.routed_scale,
+                expert_fn=lambda e: decoded_expert(W_gu, W_d, e, cfg.F))
+    t16 = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    return {"h": h, "x": x, "h_out": obf.encode(ref["h_new"]), "y": obf.encode(ref["y"]),
+            "logits": ref["logits"].astype(np.float32), "ids": ref["ids"].copy(), "wp": wp, "wq": wq,
+            "W_r": W_r, "bias": bias, "w_gu": t16(W_gu), "w_d": t16(W_d)}, ref
+
+
+def test_parity_report_counts_and_flags_disagreements():
+    import numpy as np
+    from oracle.routing import near_tie
+    cap, ref = _toy_capture()
+    rep, timing = bench.parity_report("toy", cap, workers=1)
+    assert timing is None
+    assert rep["pass"] and rep["differing_rows"] == 0 and rep["h_worst_ulp"] == 0
+    assert rep["routing_tokens"] == 16 and rep["y_tokens"] == 16 and rep["y_max_abs"] < 2e-2
+    # one token routed to another expert (not a near-tie) must fail the report
+    t = int(np.flatnonzero(~near_tie(ref["route"]))[0])
+    bad = dict(cap, ids=cap["ids"].copy())
+    bad["ids"][t, 0] = next(e for e in range(16) if e not in bad["ids"][t])
+    rep2, _ = bench.parity_report("toy", bad, workers=1)
+    assert rep2["differing_non_near_tie"] == 1 and not rep2["pass"]
+    # an h' two ulps off must fail it too
+    off = dict(cap, h_out=cap["h_out"].copy())
+    off["h_out"][3, 5] += 2
+    rep3, _ = bench.parity_report("toy", off, workers=1)
+    assert rep3["h_worst_ulp"] == 2 and not rep3["pass"]
+    # the timed variant evaluates tokens one at a time and reports its timing
+    rep4, timing = bench.parity_report("toy", cap, timed_seconds=0.0, workers=1)
+    assert timing["tokens"] == 1 and rep4["y_tokens"] == 1 and rep4["pass"]
