@@ -18,7 +18,7 @@ subset of tokens (``tokens``) and still give exact per-token results.
 """
 from __future__ import annotations
 
-from typing import Optional
+from typing import Callable, Optional
 
 import numpy as np
 
@@ -28,16 +28,23 @@ from .experts import ExpertFn, _run, swiglu_ffn
 
 
 def layer(h, x, w_post, w_pre, W_r, bias, *, n: int, eps: float, G: int, TG: int,
-          K: int, routed_scale: float, expert_fn: ExpertFn,
+          K: int, routed_scale: float, expert_fn: Optional[ExpertFn] = None,
           tokens: Optional[np.ndarray] = None, ids_override: Optional[np.ndarray] = None,
-          workers: Optional[int] = None, rule: str = "top2sum") -> dict:
+          workers: Optional[int] = None, rule: str = "top2sum",
+          ffn: Optional[Callable[[int, np.ndarray], np.ndarray]] = None) -> dict:
     """Run the sublayer on float64 inputs (bf16 values) for ``tokens`` (default: all).
 
     ``ids_override`` [len(tokens)][K] replaces the routing decision (weights
     are then recomputed from the unbiased scores of those ids); it is used to
     evaluate the layer output under another implementation's near-tie
     choices ("routing-conditioned" comparison).
+
+    The experts are the bf16 SwiGLU FFN of ``expert_fn(e)``'s matrices, or,
+    when ``ffn`` is given, ``ffn(e, rows)`` (the NVFP4 experts of
+    ``oracle.nvfp4``).
     """
+    if (expert_fn is None) == (ffn is None):
+        raise ValueError("give exactly one of expert_fn and ffn")
     h = np.asarray(h, dtype=np.float64)
     x = np.asarray(x, dtype=np.float64)
     if tokens is not None:
@@ -58,8 +65,11 @@ def layer(h, x, w_post, w_pre, W_r, bias, *, n: int, eps: float, G: int, TG: int
     def one(e: int) -> None:
         rows, slots = np.nonzero(ids == e)
         if rows.size:
-            Wg, Wu, Wd = expert_fn(e)
-            parts[e] = (rows, slots, swiglu_ffn(z[rows], Wg, Wu, Wd))
+            if ffn is not None:
+                parts[e] = (rows, slots, ffn(e, z[rows]))
+            else:
+                Wg, Wu, Wd = expert_fn(e)
+                parts[e] = (rows, slots, swiglu_ffn(z[rows], Wg, Wu, Wd))
 
     _run(one, range(E), workers)
     # the weighted sum in slot order for every token
