@@ -65,6 +65,11 @@ DEFAULT_STEPS = {"toy": 200, "decode_t1": 500, "decode_t64": 100, "prefill_t2048
 DEFAULT_BATCHES = {"toy": 16, "decode_t1": 16, "decode_t64": 16, "prefill_t2048": 4, "prefill_t16384": 2}
 # tokens whose layer output the oracle computes in the parity report (None: all)
 PARITY_Y_TOKENS = {"toy": None, "decode_t1": None, "decode_t64": 4, "prefill_t2048": 4, "prefill_t16384": 4}
+# NVFP4 experts: timed at the decode workloads after their bf16 runs (same
+# weights, quantized on the device); FP32 scales of the two quantized activations
+NVFP4_WORKLOADS = ["decode_t1", "decode_t64"]
+NVFP4_G_IN = 2.0 ** -6
+NVFP4_G_ACT = 2.0 ** -6
 # the benchmark spec tolerances, also asserted by the GPU parity tests
 TOL = {"h_ulp": 1, "logits_rel": 1e-5, "y_max_abs": 2e-2, "y_rel_l2": 5e-3, "near_tie_margin": 1e-5}
 
@@ -94,6 +99,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-parity", action="store_true", help="skip the oracle parity report")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the timed oracle sample")
+    p.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4-experts runs of the decode workloads")
+    p.add_argument("--nvfp4", action="store_true",
+                   help="with a single --config: time the layer with NVFP4 experts instead of bf16")
     args = p.parse_args(argv)
     overrides = (args.num_experts, args.tokens, args.d_ff)
     if args.config == "all" and any(v is not None for v in overrides) and args.moe_shape is None:
@@ -112,10 +120,18 @@ def parse_args(argv=None):
 
 
 def workloads(args):
-    """(workload names in run order, headline name)."""
+    """(runs in order, headline run). A run is (workload name, nvfp4)."""
     if args.config == "all":
-        return list(WORKLOADS), HEADLINE
-    return [args.config], args.config
+        runs = [(n, False) for n in WORKLOADS]
+        if not args.no_nvfp4:
+            runs += [(n, True) for n in NVFP4_WORKLOADS]
+        return runs, (HEADLINE, False)
+    return [(args.config, args.nvfp4)], (args.config, args.nvfp4)
+
+
+def run_key(run) -> str:
+    name, fp4 = run
+    return f"{name}_nvfp4" if fp4 else name
 
 
 def steps_for(args, name: str) -> int:
@@ -287,7 +303,7 @@ class DeviceWeights:
     while workloads of the same shape run (20 GB at Beam shapes)."""
 
     def __init__(self, device):
-        self.device, self.key, self.w = device, None, None
+        self.device, self.key, self.w, self.fp4 = device, None, None, None
 
     def get(self, cfg):
         import torch
@@ -304,8 +320,16 @@ class DeviceWeights:
             for e in range(E):
                 w_gu[e].copy_(torch.randn(2 * F, H, device=self.device, generator=gen) / H ** 0.5)
                 w_d[e].copy_(torch.randn(H, F, device=self.device, generator=gen) / F ** 0.5)
-            self.key, self.w = key, (w_gu, w_d)
+            self.key, self.w, self.fp4 = key, (w_gu, w_d), None
         return self.w
+
+    def nvfp4(self, cfg, beam):
+        """The current weights quantized to NVFP4 on the device (once per weight set)."""
+        w_gu, w_d = self.get(cfg)
+        if getattr(self, "fp4", None) is None:
+            mc = beam.make_config(cfg.H, cfg.E, cfg.G, cfg.TG, cfg.K, cfg.F)
+            self.fp4 = beam.beam_nvfp4_quantize_experts(w_gu, w_d, mc)
+        return self.fp4
 
 
 def device_activations(cfg, B: int, device):
@@ -336,24 +360,27 @@ def host_bits(t) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- rooflines
-def layer_floor(cfg, touched: float, peaks) -> dict:
+def layer_floor(cfg, touched: float, peaks, fp4: bool = False) -> dict:
     """The layer's roofline: algorithmic bytes (touched expert weights, router
     weight and bias, h and x read, h' and y written, z once) over the HBM peak,
-    against the expert FLOPs over the bf16 tensor peak."""
+    against the expert FLOPs over the bf16 tensor peak (for NVFP4 experts the
+    weights are codes plus scales and the FLOPs run at the FP4 rate, 4x bf16)."""
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
-    bytes_ = touched * 3 * F * H * 2 + E * H * 4 + E * 4 + 5 * T * H * 2
+    per_expert = (3 * F * H // 2 + 3 * F * H // 16) if fp4 else 3 * F * H * 2
+    bytes_ = touched * per_expert + E * H * 4 + E * 4 + 5 * T * H * 2
     flops = 2.0 * T * K * 3 * H * F
     t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12 * (4 if fp4 else 1))
     return {"bound": "hbm" if t_hbm >= t_tc else "tensor", "algorithmic_bytes": bytes_, "expert_flops": flops,
             "floor_us": 1e6 * max(t_hbm, t_tc)}
 
 
 # ---------------------------------------------------------------- one workload on the GPU
-def measure(name, args, env, world):
-    """Times one workload; returns (report dict, capture of batch 0 for the
-    parity check)."""
+def measure(run, args, env, world):
+    """Times one workload (bf16 or NVFP4 experts); returns (report dict,
+    capture of batch 0 for the parity check)."""
     import torch
+    name, fp4 = run
     lib, beam, device = env["lib"], env["beam"], env["device"]
     cfg = CONFIGS[name]
     T, H, E, F = cfg.T, cfg.H, cfg.E, cfg.F
@@ -367,7 +394,14 @@ def measure(name, args, env, world):
     W_r, bias = make_router(cfg)
     tens = dict(w_post=bf(wp), w_pre=bf(wq), router_w=torch.from_numpy(W_r).to(device),
                 bias=torch.from_numpy(bias).to(device), w_gate_up=w_gu, w_down=w_d)
-    weights = beam.weights_struct(**tens)
+    if fp4:
+        ex = env["weights"].nvfp4(cfg, beam)
+        weights = beam.nvfp4_weights_struct(tens["w_post"], tens["w_pre"], tens["router_w"], tens["bias"], ex,
+                                            NVFP4_G_IN, NVFP4_G_ACT)
+        layer_fn, ws_fn = lib.beam_moe_layer_nvfp4, lib.beam_moe_nvfp4_workspace_size
+    else:
+        weights = beam.weights_struct(**tens)
+        layer_fn, ws_fn = lib.beam_moe_layer, lib.beam_moe_workspace_size
 
     B = batches_for(args, name)
     K, W = steps_for(args, name), args.warmup
@@ -378,7 +412,7 @@ def measure(name, args, env, world):
     h_out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
     y_out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
     offs = torch.empty(E + 1, dtype=torch.int32, device=device)
-    ws_bytes = lib.beam_moe_workspace_size(ctypes.byref(mc), T)
+    ws_bytes = ws_fn(ctypes.byref(mc), T)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     flush_l2 = env["flush_l2"]
     stream = torch.cuda.current_stream(device)
@@ -405,11 +439,10 @@ def measure(name, args, env, world):
 
     def step(i, dbg):
         b = i % B
-        st = lib.beam_moe_layer(hs[b].data_ptr(), xs[b].data_ptr(), cfg.n, ctypes.byref(weights), T,
-                                ctypes.byref(mc), h_out.data_ptr(), y_out.data_ptr(), ctypes.byref(dbg),
-                                ws.data_ptr(), ws_bytes, sp)
+        st = layer_fn(hs[b].data_ptr(), xs[b].data_ptr(), cfg.n, ctypes.byref(weights), T, ctypes.byref(mc),
+                      h_out.data_ptr(), y_out.data_ptr(), ctypes.byref(dbg), ws.data_ptr(), ws_bytes, sp)
         if st != 0:
-            raise RuntimeError(f"beam_moe_layer ({name}): {beam.beam_status_string(st)}")
+            raise RuntimeError(f"layer ({run_key(run)}): {beam.beam_status_string(st)}")
 
     # warm-up; also records how many experts each batch touches
     touched = []
@@ -431,11 +464,11 @@ def measure(name, args, env, world):
         for b in range(B):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=gstream):
-                st = lib.beam_moe_layer(hs[b].data_ptr(), xs[b].data_ptr(), cfg.n, ctypes.byref(weights), T,
-                                        ctypes.byref(mc), h_out.data_ptr(), y_out.data_ptr(), None,
-                                        ws.data_ptr(), ws_bytes, gstream.cuda_stream)
+                st = layer_fn(hs[b].data_ptr(), xs[b].data_ptr(), cfg.n, ctypes.byref(weights), T,
+                              ctypes.byref(mc), h_out.data_ptr(), y_out.data_ptr(), None, ws.data_ptr(), ws_bytes,
+                              gstream.cuda_stream)
             if st != 0:
-                raise RuntimeError(f"beam_moe_layer (capture, {name}): {beam.beam_status_string(st)}")
+                raise RuntimeError(f"layer (capture, {run_key(run)}): {beam.beam_status_string(st)}")
             graphs.append(g)
         for i in range(W):
             flush_l2()
@@ -474,7 +507,7 @@ def measure(name, args, env, world):
         torch.cuda.synchronize()
         other_ms = [gev[i][0].elapsed_time(gev[i][1]) for i in range(K2)]
     next_boundary = deferred_combine_report(K, lib, beam, cfg, mc, weights, tens, hs, xs, ws, ws_bytes, B,
-                                            flush_l2, device) if graphs else None
+                                            flush_l2, device) if graphs and not fp4 else None
     del graphs
     barrier()
     for i in range(K2):
@@ -510,7 +543,14 @@ def measure(name, args, env, world):
     # as the gate/up stage and the down stage is empty: the dominant kernel is
     # then the fused one and its algorithmic bytes cover both weight sets.
     fused = mean_stage["down"] < 0.05 * mean_stage["gate_up"]
-    if fused:
+    if fp4:
+        # NVFP4: codes (half a byte per weight) plus one E4M3 scale per 16
+        # weights; the input and SwiGLU rows as codes and scale slots, y_perm bf16
+        dom = "experts_fused_nvfp4"
+        w_bytes = 3 * F * H // 2 + 3 * F * H // 16
+        act_bytes = rows * (H // 2 + H // 4) + 2 * rows * (F // 2 + F // 4) + rows * H * 2
+        flops = 2.0 * rows * 3 * F * H
+    elif fused:
         dom = "experts_fused"
         w_bytes = 3 * F * H * 2
         act_bytes = rows * H * 2 + 2 * rows * F * 2 + rows * H * 2
@@ -526,7 +566,7 @@ def measure(name, args, env, world):
             act_bytes = rows * F * 2 + rows * H * 2
             flops = 2.0 * rows * H * F
     bytes_total = sum(tc * w_bytes + act_bytes for tc in touched_per_step)
-    dom_stage = "gate_up" if fused else dom
+    dom_stage = "gate_up" if (fused or fp4) else dom
     dom_s = sum(stage_ms[dom_stage]) / 1e3
     t_hbm = bytes_total / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops * K2 / (peaks["bf16_tflops"] * 1e12)
@@ -548,13 +588,14 @@ def measure(name, args, env, world):
     expert_flops = 2.0 * rows * 3 * F * H
     expert_gemms = {"us": 1e6 * gemm_s, "tflops": expert_flops / gemm_s / 1e12, "peak": peaks[tc_key],
                     "peak_source": tc_kind, "frac_of_bf16_peak": expert_flops / gemm_s / 1e12 / peaks[tc_key]}
-    floor = layer_floor(cfg, statistics.fmean(touched_per_step), peaks)
+    floor = layer_floor(cfg, statistics.fmean(touched_per_step), peaks, fp4)
     floor["frac"] = floor["floor_us"] / us_per_layer
     floor["peak_source"] = peaks_kind
 
     # end to end through the host-buffer entry point: H2D of h, x and D2H of h', y inside the timed region
+    # (the host-buffer entry point takes bf16 experts: no end-to-end number for NVFP4)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not fp4:
         hbytes = lib.beam_moe_layer_host_workspace_size(ctypes.byref(mc), T)
         ws_h = torch.empty(hbytes, dtype=torch.uint8, device=device)
         ho = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
@@ -600,7 +641,9 @@ def measure(name, args, env, world):
                "logits": dbg["logits"].cpu().numpy(), "ids": dbg["topk_ids"].cpu().numpy(),
                "wp": wp, "wq": wq, "W_r": W_r, "bias": bias, "w_gu": w_gu, "w_d": w_d}
 
-    report = {"workload": name, "T": T, "tokens_per_s": value, "us_per_layer": us_per_layer,
+    capture["nvfp4"] = fp4
+    report = {"workload": name, "experts": "nvfp4" if fp4 else "bf16", "T": T, "tokens_per_s": value,
+              "us_per_layer": us_per_layer,
               "ms_per_step": 1e3 * slowest / K, "steps": K, "warmup": W, "batches": B,
               "timing": ("CUDA-graph replay of the whole layer per step (one graph per seeded batch), events "
                          "on the replay stream" if graph_ms else "direct launches, events on the launch stream"),
@@ -658,12 +701,24 @@ def parity_report(name, cap, timed_seconds=None, workers=None):
     Lg = cap["logits"][tokens].astype(np.float64)
     logit_rel = float(np.max(np.abs(Lg - L).max(axis=1) / np.maximum(np.abs(L).max(axis=1), 1e-300)))
 
-    # layer output on the first few tokens of the sample
-    ny = PARITY_Y_TOKENS.get(name)
+    # layer output on the first few tokens of the sample (one token with NVFP4
+    # experts, whose oracle quantizes each touched expert on the host first)
+    fp4 = cap.get("nvfp4", False)
+    ny = 1 if fp4 else PARITY_Y_TOKENS.get(name)
     ysel = tokens if ny is None else tokens[:ny]
     efn = expert_reader(cap["w_gu"], cap["w_d"], cfg.F)
     common = dict(n=cfg.n, eps=cfg.eps, G=cfg.G, TG=cfg.TG, K=cfg.K, routed_scale=cfg.routed_scale,
-                  expert_fn=efn, workers=workers)
+                  workers=workers)
+    if fp4:
+        from oracle import nvfp4 as onv
+
+        def ffn(e, X):
+            Wg, Wu, Wd = efn(e)
+            ex = onv.Nvfp4Expert(Wg.astype(np.float32), Wu.astype(np.float32), Wd.astype(np.float32))
+            return onv.ffn(X, ex, NVFP4_G_IN, NVFP4_G_ACT)
+        common["ffn"] = ffn
+    else:
+        common["expert_fn"] = efn
     args_l = (obf.decode(cap["h"]), obf.decode(cap["x"]), wp64, wq64, cap["W_r"], cap["bias"])
     timing = None
     if timed_seconds is None:
@@ -712,7 +767,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    _, headline = workloads(args)
+    _, (headline, _) = workloads(args)
     cfg = CONFIGS[headline]
     from beam_inputs import expert_weights, make_activations
     from oracle import bf16 as obf
@@ -789,19 +844,21 @@ def run_ours(args):
             flush_words.sum()
 
     env = {"lib": lib, "beam": beam, "device": device, "flush_l2": flush_l2, "weights": DeviceWeights(device)}
-    names, headline = workloads(args)
+    runs, head_run = workloads(args)
     reports, captures = {}, {}
-    for name in names:
-        reports[name], captures[name] = measure(name, args, env, world)
+    for run in runs:
+        key = run_key(run)
+        reports[key], captures[key] = measure(run, args, env, world)
         torch.cuda.empty_cache()
 
     # parity against the oracle (and the timed oracle sample) on rank 0 of a 1-GPU run
     cpu = None
     if rank == 0 and world == 1 and not args.no_parity:
-        for name in names:
-            timed = (not args.no_cpu_baseline) and name == headline
-            rep, timing = parity_report(name, captures[name], timed_seconds=args.cpu_seconds if timed else None)
-            reports[name]["parity"] = rep
+        for run in runs:
+            key, name = run_key(run), run[0]
+            timed = (not args.no_cpu_baseline) and run == head_run
+            rep, timing = parity_report(name, captures[key], timed_seconds=args.cpu_seconds if timed else None)
+            reports[key]["parity"] = rep
             if timing is not None:
                 cpu = {"value": timing["tokens"] / timing["seconds"], "unit": UNIT, "cores": timing["workers"],
                        "kind": "oracle",
@@ -811,7 +868,8 @@ def run_ours(args):
     captures.clear()
 
     if rank == 0:
-        head = reports[headline]
+        headline = head_run[0]
+        head = reports[run_key(head_run)]
         cfg = CONFIGS[headline]
         B = batches_for(args, headline)
         l2 = ("512 MB buffer overwritten " + ("and read back " if args.l2_flush == "write-read" else "")
@@ -824,7 +882,7 @@ def run_ours(args):
                "layer_roofline": head["layer_roofline"], "expert_gemms": head["expert_gemms"],
                "cpu_baseline": cpu, "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
                "clocks": head["clocks"],
-               "parity": {n: reports[n].get("parity") for n in names},
+               "parity": {k: reports[k].get("parity") for k in reports},
                "parity_tolerances": TOL,
                "per_config": reports}
         print(json.dumps(out), flush=True)

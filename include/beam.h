@@ -234,6 +234,98 @@ beam_status_t beam_boundary_norm_combine(const uint16_t* h, const uint16_t* y_pe
                                          int H, float eps, int n, uint16_t* h_out,
                                          uint16_t* z_out, void* stream);
 
+/* ------------------------------------------------------------------ NVFP4 experts
+ * The expert GEMMs on 4-bit weights and inputs (TokenSpeed blog, "Model
+ * architecture and precision -> NVFP4 and FP8 checkpoints": each expert weight
+ * is an E2M1 value, every 16 weights share an E4M3 scale and each expert has
+ * an additional FP32 scale; expert inputs are quantized in the same format at
+ * runtime, so the GEMMs run FP4 x FP4; "TensorRT-LLM NVFP4 MoE": the kernel
+ * reads about a quarter of the BF16 weight bytes). Block-scaled tcgen05 MMAs.
+ *
+ * One block = 16 consecutive values along the reduction dimension of a row.
+ * With FP32 scale g, its scale is s = E4M3(amax / (6 g)) and each value's code
+ * q = E2M1(x / (s g)), both rounded to nearest even and saturating (448, 6),
+ * every product and quotient in FP32; the value represented is q * s * g. An
+ * expert's g is its largest |w| over gate, up and down divided by 6 * 448.
+ * Codes are stored two per byte, element 2j in the low nibble.
+ *
+ * Weight layouts (produced by beam_nvfp4_quantize_experts):
+ *   q_gate_up  uint8 [E][2F][H/2]  (rows 0..F-1 gate, F..2F-1 up)
+ *   q_down     uint8 [E][H][F/2]
+ *   sf_gate_up uint8 [2E][F/128][H/256][4][512]: plane 2e = expert e's gate
+ *              rows, 2e+1 its up rows; per 128-row block and 256-value k-step
+ *              four 512-byte atoms (one per 64 values); in atom c, byte
+ *              (r%32)*16 + (r/32)*4 + j is the scale of row r (0..127 in the
+ *              block), values 64c + 16j .. +15 of the k-step
+ *   sf_down    uint8 [E][H/128][F/256][4][512], the same arrangement
+ *   expert_scale float [E]
+ * Activation layout (beam_nvfp4_quantize_rows and the layer's internal
+ * buffers): codes uint8 [rows][K/2]; scales uint8 [rows][K/64][16], one
+ * 16-byte slot per 64 values whose bytes 0..3 are the four 16-value scales
+ * (bytes 4..15 are never read; beam_nvfp4_quantize_rows writes zeros there).
+ * Shapes: H % 256 == 0, F % 256 == 0, E <= 256. */
+typedef struct {
+  const uint16_t* w_post;      /* bf16 [H] */
+  const uint16_t* w_pre;       /* bf16 [H] */
+  const float* router_w;       /* fp32 [E][H] */
+  const float* bias;           /* fp32 [E] */
+  const uint8_t* q_gate_up;    /* see above */
+  const uint8_t* sf_gate_up;
+  const uint8_t* q_down;
+  const uint8_t* sf_down;
+  const float* expert_scale;   /* [E] */
+  float input_scale;           /* FP32 scale of the quantized expert input (the pre-normed z), > 0 */
+  float act_scale;             /* FP32 scale of the quantized SwiGLU output (the down GEMM's input), > 0 */
+} beam_moe_nvfp4_weights_t;
+
+/* Sizes in bytes of the four weight arrays (any pointer may be NULL);
+ * returns their total plus the expert scales, 0 for an unsupported config. */
+size_t beam_nvfp4_expert_bytes(const beam_moe_config_t* cfg, size_t* q_gate_up, size_t* sf_gate_up,
+                               size_t* q_down, size_t* sf_down);
+
+/* Quantizes bf16 expert weights (the beam_moe_weights_t layouts) to the NVFP4
+ * layouts above: one pass for each expert's largest |w|, one that writes
+ * codes and scales, one for the expert scales. Every output is written. */
+beam_status_t beam_nvfp4_quantize_experts(const uint16_t* w_gate_up, const uint16_t* w_down,
+                                          const beam_moe_config_t* cfg, uint8_t* q_gate_up,
+                                          uint8_t* sf_gate_up, uint8_t* q_down, uint8_t* sf_down,
+                                          float* expert_scale, void* stream);
+
+/* Runtime quantization of bf16 rows x [rows][K] with FP32 scale `scale`
+ * (K % 64 == 0): codes q [rows][K/2], scale slots sf [rows][K/64][16]. */
+beam_status_t beam_nvfp4_quantize_rows(const uint16_t* x, int rows, int K, float scale, uint8_t* q,
+                                       uint8_t* sf, void* stream);
+
+/* The NVFP4 experts stage: x_perm (bf16 [T*K][H], beam_moe_permute's rows)
+ * quantized with input_scale; per expert, act = silu(gate) * up from the
+ * block-scaled gate/up GEMM times the expert and input scales, quantized
+ * with act_scale; y_perm = bf16(act GEMM W_down times the expert and act
+ * scales); the combine as in beam_moe_experts. y_out bf16 [T][H]. `inter`
+ * (may be NULL) receives the workspace addresses of the intermediates,
+ * valid until `ws` is next used. */
+typedef struct {
+  const uint8_t* x_q;       /* [T*K][H/2] */
+  const uint8_t* x_sf;      /* [T*K][H/64][16] */
+  const uint8_t* act_q;     /* [T*K][F/2] */
+  const uint8_t* act_sf;    /* [T*K][F/64][16] */
+  const uint16_t* y_perm;   /* bf16 [T*K][H] */
+} beam_moe_nvfp4_intermediates_t;
+size_t beam_moe_experts_nvfp4_workspace_size(const beam_moe_config_t* cfg, int T);
+beam_status_t beam_moe_experts_nvfp4(const uint16_t* x_perm, const int32_t* expert_offsets,
+                                     const beam_moe_nvfp4_weights_t* weights, const float* topk_w,
+                                     const int32_t* inv_perm, int T, const beam_moe_config_t* cfg,
+                                     uint16_t* y_out, beam_moe_nvfp4_intermediates_t* inter, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/* beam_moe_layer with NVFP4 experts: the same boundary, FP32 routing and
+ * permutation, then beam_moe_experts_nvfp4. dbg as for beam_moe_layer (its
+ * stage event [3] is recorded after the input quantization). */
+size_t beam_moe_nvfp4_workspace_size(const beam_moe_config_t* cfg, int T);
+beam_status_t beam_moe_layer_nvfp4(const uint16_t* h, const uint16_t* x, int n,
+                                   const beam_moe_nvfp4_weights_t* weights, int T,
+                                   const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
+                                   const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream);
+
 /* beam_moe_layer with HOST input and output buffers: copies h and x (host,
  * pinned memory recommended) into the workspace, runs the layer, copies h_out
  * and y_out back to the host buffers, and synchronises the stream before it

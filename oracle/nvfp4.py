@@ -78,12 +78,14 @@ def _nearest_even(a: np.ndarray, mags: np.ndarray) -> np.ndarray:
     ties to the even index (the code whose last mantissa bit is 0); values
     above the largest saturate to it."""
     a = np.minimum(np.asarray(a, dtype=np.float64), mags[-1])
-    hi = np.clip(np.searchsorted(mags, a, side="left"), 0, mags.size - 1)  # first value >= a
+    hi = np.searchsorted(mags, a, side="left")          # first value >= a
+    np.minimum(hi, mags.size - 1, out=hi)
     lo = np.maximum(hi - 1, 0)
     dlo, dhi = a - mags[lo], mags[hi] - a
     # the nearer neighbour; at equal distance the one with the even index
-    tie_pick = np.where(lo % 2 == 0, lo, hi)
-    return np.where(dhi < dlo, hi, np.where(dlo < dhi, lo, tie_pick))
+    # (of two neighbours exactly one is even: the upper one when lo is odd)
+    take_hi = (dhi < dlo) | ((dhi == dlo) & (lo % 2 == 1))
+    return np.where(take_hi, hi, lo)
 
 
 def e2m1_round(v) -> np.ndarray:
@@ -91,8 +93,9 @@ def e2m1_round(v) -> np.ndarray:
     sign bit is the value's, as in IEEE rounding: a negative value that
     rounds to zero gives -0 (code 8)."""
     v = np.asarray(v, dtype=np.float64)
-    code = _nearest_even(np.abs(v), _E2M1_MAGS)
-    return np.where(np.signbit(v), code | 8, code).astype(np.uint8)
+    code = _nearest_even(np.abs(v), _E2M1_MAGS).astype(np.uint8)
+    code |= np.signbit(v).astype(np.uint8) << 3
+    return code
 
 
 def e4m3_round(v) -> np.ndarray:

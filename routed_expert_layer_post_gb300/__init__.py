@@ -27,7 +27,9 @@ __all__ = [
     "beam_moe_workspace_size", "beam_moe_permute_workspace_size",
     "beam_moe_experts_workspace_size", "beam_moe_layer_host_workspace_size",
     "beam_get_device_error", "beam_check_bounded_wait", "beam_check_bounded_wait_pending",
-    "beam_release_host_graphs", "beam_last_launch_count", "beam_status_string", "Workspace",
+    "beam_release_host_graphs", "MoeNvfp4Weights", "MoeNvfp4Intermediates", "Nvfp4Experts",
+    "beam_nvfp4_quantize_experts", "beam_nvfp4_quantize_rows", "nvfp4_weights_struct", "beam_moe_experts_nvfp4",
+    "beam_moe_layer_nvfp4", "beam_moe_nvfp4_workspace_size", "beam_last_launch_count", "beam_status_string", "Workspace",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbeam.so")
@@ -57,6 +59,17 @@ class MoeDebug(ctypes.Structure):
 
 class MoeUncombined(ctypes.Structure):
     _fields_ = [("y_perm", c_void_p), ("topk_w", c_void_p), ("inv_perm", c_void_p)]
+
+
+class MoeNvfp4Weights(ctypes.Structure):
+    _fields_ = [("w_post", c_void_p), ("w_pre", c_void_p), ("router_w", c_void_p), ("bias", c_void_p),
+                ("q_gate_up", c_void_p), ("sf_gate_up", c_void_p), ("q_down", c_void_p), ("sf_down", c_void_p),
+                ("expert_scale", c_void_p), ("input_scale", c_float), ("act_scale", c_float)]
+
+
+class MoeNvfp4Intermediates(ctypes.Structure):
+    _fields_ = [("x_q", c_void_p), ("x_sf", c_void_p), ("act_q", c_void_p), ("act_sf", c_void_p),
+                ("y_perm", c_void_p)]
 
 
 def make_config(hidden: int, num_experts: int, num_groups: int, topk_groups: int, topk: int,
@@ -103,6 +116,20 @@ _SIGNATURES = {
     "beam_release_host_graphs": (c_int, []),
     "beam_moe_permute_no_alloc": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeConfig), c_void_p,
                                           c_void_p, c_void_p, c_void_p, c_void_p]),
+    "beam_nvfp4_expert_bytes": (c_size_t, [ctypes.POINTER(MoeConfig), ctypes.POINTER(c_size_t),
+                                           ctypes.POINTER(c_size_t), ctypes.POINTER(c_size_t),
+                                           ctypes.POINTER(c_size_t)]),
+    "beam_nvfp4_quantize_experts": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeConfig), c_void_p, c_void_p,
+                                            c_void_p, c_void_p, c_void_p, c_void_p]),
+    "beam_nvfp4_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_float, c_void_p, c_void_p, c_void_p]),
+    "beam_moe_experts_nvfp4_workspace_size": (c_size_t, [ctypes.POINTER(MoeConfig), c_int]),
+    "beam_moe_experts_nvfp4": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeNvfp4Weights), c_void_p, c_void_p,
+                                       c_int, ctypes.POINTER(MoeConfig), c_void_p,
+                                       ctypes.POINTER(MoeNvfp4Intermediates), c_void_p, c_size_t, c_void_p]),
+    "beam_moe_nvfp4_workspace_size": (c_size_t, [ctypes.POINTER(MoeConfig), c_int]),
+    "beam_moe_layer_nvfp4": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeNvfp4Weights), c_int,
+                                     ctypes.POINTER(MoeConfig), c_void_p, c_void_p, ctypes.POINTER(MoeDebug),
+                                     c_void_p, c_size_t, c_void_p]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -280,9 +307,13 @@ def beam_moe_combine(y_perm, topk_w, inv_perm, cfg: MoeConfig, T: int, y_out=Non
 
 
 def weights_struct(w_post, w_pre, router_w, bias, w_gate_up, w_down) -> MoeWeights:
+    """The weights as the C struct of device pointers; the struct keeps the
+    tensors alive for as long as it lives."""
     bf = torch.bfloat16
-    return MoeWeights(_p(w_post, bf), _p(w_pre, bf), _p(router_w, torch.float32), _p(bias, torch.float32),
-                      _p(w_gate_up, bf), _p(w_down, bf))
+    s = MoeWeights(_p(w_post, bf), _p(w_pre, bf), _p(router_w, torch.float32), _p(bias, torch.float32),
+                   _p(w_gate_up, bf), _p(w_down, bf))
+    s._keep = (w_post, w_pre, router_w, bias, w_gate_up, w_down)
+    return s
 
 
 def beam_moe_layer(h, x, n: int, weights: MoeWeights, cfg: MoeConfig, h_out=None, y_out=None,
@@ -399,3 +430,100 @@ def beam_check_bounded_wait_pending(limit_ms: int = 50) -> None:
     flag = torch.zeros(4, dtype=torch.int32, device="cuda")
     _check("beam_check_bounded_wait_pending",
            library().beam_check_bounded_wait_pending(flag.data_ptr(), limit_ms, _stream()))
+
+
+# ---------------------------------------------------------------- NVFP4 experts
+class Nvfp4Experts:
+    """Device tensors of NVFP4 expert weights (layouts in beam.h): codes and
+    scale atoms of gate/up and down, and the per-expert FP32 scales."""
+
+    def __init__(self, q_gate_up, sf_gate_up, q_down, sf_down, expert_scale):
+        self.q_gate_up, self.sf_gate_up = q_gate_up, sf_gate_up
+        self.q_down, self.sf_down = q_down, sf_down
+        self.expert_scale = expert_scale
+
+
+def beam_nvfp4_quantize_experts(w_gate_up, w_down, cfg: MoeConfig) -> Nvfp4Experts:
+    """Quantizes bf16 expert weights [E][2F][H] and [E][H][F] to NVFP4."""
+    sizes = [c_size_t(0) for _ in range(4)]
+    if library().beam_nvfp4_expert_bytes(ctypes.byref(cfg), *(ctypes.byref(v) for v in sizes)) == 0:
+        raise BeamError("beam_nvfp4_expert_bytes: unsupported config")
+    dev = w_gate_up.device
+    bufs = [torch.empty(v.value, dtype=torch.uint8, device=dev) for v in sizes]
+    scale = torch.empty(cfg.num_experts, dtype=torch.float32, device=dev)
+    bf = torch.bfloat16
+    _check("beam_nvfp4_quantize_experts", library().beam_nvfp4_quantize_experts(
+        _p(w_gate_up, bf), _p(w_down, bf), ctypes.byref(cfg), *(b.data_ptr() for b in bufs), scale.data_ptr(),
+        _stream()))
+    return Nvfp4Experts(bufs[0], bufs[1], bufs[2], bufs[3], scale)
+
+
+def beam_nvfp4_quantize_rows(x, scale: float):
+    """bf16 rows [R][K] -> (codes uint8 [R][K/2], scale slots uint8 [R][K/64][16])."""
+    R, K = x.shape
+    q = torch.empty(R, K // 2, dtype=torch.uint8, device=x.device)
+    sf = torch.empty(R, K // 64, 16, dtype=torch.uint8, device=x.device)
+    _check("beam_nvfp4_quantize_rows", library().beam_nvfp4_quantize_rows(
+        _p(x, torch.bfloat16), R, K, scale, q.data_ptr(), sf.data_ptr(), _stream()))
+    return q, sf
+
+
+def nvfp4_weights_struct(w_post, w_pre, router_w, bias, experts: Nvfp4Experts, input_scale: float,
+                         act_scale: float) -> MoeNvfp4Weights:
+    bf = torch.bfloat16
+    s = MoeNvfp4Weights(_p(w_post, bf), _p(w_pre, bf), _p(router_w, torch.float32), _p(bias, torch.float32),
+                        _p(experts.q_gate_up, torch.uint8), _p(experts.sf_gate_up, torch.uint8),
+                        _p(experts.q_down, torch.uint8), _p(experts.sf_down, torch.uint8),
+                        _p(experts.expert_scale, torch.float32), input_scale, act_scale)
+    s._keep = (w_post, w_pre, router_w, bias, experts)  # the struct holds raw pointers: keep the tensors alive
+    return s
+
+
+def beam_moe_experts_nvfp4(x_perm, offsets, weights: MoeNvfp4Weights, topk_w, inv_perm, cfg: MoeConfig, T: int,
+                           y_out=None, ws: Optional[Workspace] = None):
+    """The NVFP4 experts stage. Returns (y bf16 [T][H], intermediates dict of
+    workspace views: x_q, x_sf, act_q, act_sf, y_perm)."""
+    y_out = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=x_perm.device) if y_out is None else y_out
+    buf = _ws(library().beam_moe_experts_nvfp4_workspace_size(ctypes.byref(cfg), T), ws)
+    inter = MoeNvfp4Intermediates()
+    _check("beam_moe_experts_nvfp4", library().beam_moe_experts_nvfp4(
+        _p(x_perm, torch.bfloat16), _p(offsets, torch.int32), ctypes.byref(weights), _p(topk_w, torch.float32),
+        _p(inv_perm, torch.int32), T, ctypes.byref(cfg), _p(y_out, torch.bfloat16), ctypes.byref(inter),
+        buf.data_ptr(), buf.numel(), _stream()))
+    if T == 0:
+        return y_out, None
+    rows, H, F = T * cfg.topk, cfg.hidden, cfg.d_ff
+    views = {"x_q": _ws_view(buf, inter.x_q, torch.uint8, (rows, H // 2)),
+             "x_sf": _ws_view(buf, inter.x_sf, torch.uint8, (rows, H // 64, 16)),
+             "act_q": _ws_view(buf, inter.act_q, torch.uint8, (rows, F // 2)),
+             "act_sf": _ws_view(buf, inter.act_sf, torch.uint8, (rows, F // 64, 16)),
+             "y_perm": _ws_view(buf, inter.y_perm, torch.bfloat16, (rows, H))}
+    return y_out, views
+
+
+def beam_moe_nvfp4_workspace_size(cfg: MoeConfig, T: int) -> int:
+    return library().beam_moe_nvfp4_workspace_size(ctypes.byref(cfg), T)
+
+
+def beam_moe_layer_nvfp4(h, x, n: int, weights: MoeNvfp4Weights, cfg: MoeConfig, h_out=None, y_out=None,
+                         debug: bool = False, ws: Optional[Workspace] = None):
+    """One MoE sublayer with NVFP4 experts. Returns (h_out, y, dbg) as beam_moe_layer."""
+    T = h.shape[0]
+    dev = h.device
+    h_out = torch.empty_like(h) if h_out is None else h_out
+    y_out = torch.empty_like(h) if y_out is None else y_out
+    dbg, dbg_struct = None, None
+    if debug:
+        dbg = {"z": torch.empty_like(h),
+               "logits": torch.empty(T, cfg.num_experts, dtype=torch.float32, device=dev),
+               "topk_ids": torch.empty(T, cfg.topk, dtype=torch.int32, device=dev),
+               "topk_w": torch.empty(T, cfg.topk, dtype=torch.float32, device=dev),
+               "expert_offsets": torch.empty(cfg.num_experts + 1, dtype=torch.int32, device=dev)}
+        dbg_struct = MoeDebug(*(dbg[k].data_ptr() for k in ("z", "logits", "topk_ids", "topk_w",
+                                                             "expert_offsets")))
+    buf = _ws(beam_moe_nvfp4_workspace_size(cfg, T), ws)
+    bf = torch.bfloat16
+    _check("beam_moe_layer_nvfp4", library().beam_moe_layer_nvfp4(
+        _p(h, bf), _p(x, bf), n, ctypes.byref(weights), T, ctypes.byref(cfg), _p(h_out, bf), _p(y_out, bf),
+        ctypes.byref(dbg_struct) if dbg_struct is not None else None, buf.data_ptr(), buf.numel(), _stream()))
+    return h_out, y_out, dbg

@@ -17,7 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbeam.so")
-SOURCES = ["api.cu", "boundary.cu", "router.cu", "permute.cu", "experts.cu", "permute_no_alloc.cu", "route_decode.cu"]
+SOURCES = ["api.cu", "boundary.cu", "router.cu", "permute.cu", "experts.cu", "permute_no_alloc.cu", "route_decode.cu",
+           "nvfp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

@@ -103,11 +103,32 @@ ExpertsWs experts_ws(const beam_moe_config_t* c, int T, int sms) {
   return w;
 }
 
+// NVFP4 experts stage: the quantized input rows, the quantized SwiGLU output,
+// the bf16 down output and the GEMM scratch of the NVFP4 plans.
+struct ExpertsWsFp4 {
+  size_t xq, xsf, act_q, act_sf, y_perm, gemm, total;
+};
+
+ExpertsWsFp4 experts_ws_fp4(const beam_moe_config_t* c, int T, int sms) {
+  ExpertsWsFp4 w{};
+  const size_t rows = static_cast<size_t>(T) * c->topk;
+  beam::GemmPlan p0, p1;
+  beam::plan_experts(T, c->topk, c->num_experts, c->hidden, c->d_ff, sms, &p0, &p1, /*fp4=*/true);
+  w.xq = 0;
+  w.xsf = align_up(w.xq + rows * c->hidden / 2);
+  w.act_q = align_up(w.xsf + rows * c->hidden / 4);
+  w.act_sf = align_up(w.act_q + rows * c->d_ff / 2);
+  w.y_perm = align_up(w.act_sf + rows * c->d_ff / 4);
+  w.gemm = align_up(w.y_perm + rows * c->hidden * 2);
+  w.total = align_up(w.gemm + beam::gemm_scratch_bytes(p0, p1));
+  return w;
+}
+
 struct LayerWs {
   size_t z, logits, ids, w, offsets, perm, inv, perm_scratch, router_ticket, router_w3, x_perm, experts, total;
 };
 
-LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
+LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms, bool fp4 = false) {
   LayerWs l{};
   const size_t rows = static_cast<size_t>(T) * c->topk;
   size_t o = 0;
@@ -124,7 +145,7 @@ LayerWs layer_ws(const beam_moe_config_t* c, int T, int sms) {
   if (beam::router_tc_supported(T, c->num_experts, c->hidden))
     o = align_up(o + beam::router_tc_scratch_bytes(c->num_experts, c->hidden));
   l.x_perm = o;       o = align_up(o + rows * c->hidden * 2);
-  l.experts = o;      o = align_up(o + experts_ws(c, T, sms).total);
+  l.experts = o;      o = align_up(o + (fp4 ? experts_ws_fp4(c, T, sms).total : experts_ws(c, T, sms).total));
   l.total = o;
   return l;
 }
@@ -179,6 +200,60 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
     e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, /*pdl=*/true, err_out);
   record(dbg, 6, s);
   return cuda_status(e);
+}
+
+// The NVFP4 experts stage: the bf16 input rows quantized (FP32 scale g_in),
+// both GEMMs in one launch (the SwiGLU output quantized with g_act), then
+// the combine. `cleared`: the GEMM counters and tickets were zeroed by an
+// earlier kernel. `inter` (optional) receives the workspace addresses of the
+// intermediates.
+beam_status_t run_experts_fp4(const uint16_t* x_perm, const int32_t* offsets, const beam::Nvfp4Experts& wt,
+                              float g_in, float g_act, const float* topk_w, const int32_t* inv, int T,
+                              const beam_moe_config_t* c, uint16_t* y, char* ws, int sms, cudaStream_t s,
+                              const beam_moe_debug_t* dbg, bool pdl, bool cleared, int* err_out,
+                              beam_moe_nvfp4_intermediates_t* inter) {
+  const ExpertsWsFp4 w = experts_ws_fp4(c, T, sms);
+  const int rows = T * c->topk;
+  uint8_t* xq = reinterpret_cast<uint8_t*>(ws + w.xq);
+  uint8_t* xsf = reinterpret_cast<uint8_t*>(ws + w.xsf);
+  uint8_t* aq = reinterpret_cast<uint8_t*>(ws + w.act_q);
+  uint8_t* asf = reinterpret_cast<uint8_t*>(ws + w.act_sf);
+  uint16_t* y_perm = reinterpret_cast<uint16_t*>(ws + w.y_perm);
+  void* g = ws + w.gemm;
+  if (inter != nullptr) *inter = beam_moe_nvfp4_intermediates_t{xq, xsf, aq, asf, y_perm};
+  beam::GemmPlan p0, p1;
+  beam::plan_experts(T, c->topk, c->num_experts, c->hidden, c->d_ff, sms, &p0, &p1, /*fp4=*/true);
+  cudaError_t e = cudaSuccess;
+  if (!cleared && (e = beam::clear_gemm_scratch(g, p0, p1, s)) != cudaSuccess) return BEAM_ERR_CUDA;
+  if ((e = beam::launch_quantize_rows(x_perm, rows, c->hidden, g_in, xq, xsf, s, pdl)) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(dbg, 3, s);
+  e = beam::launch_fused_experts_fp4(p0, p1, wt, xq, xsf, g_in, offsets, rows, c->num_experts, c->hidden, c->d_ff,
+                                     aq, asf, g_act, y_perm, g, sms, s, pdl);
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  record(dbg, 4, s);
+  record(dbg, 5, s);
+  if (y != nullptr)
+    e = beam::launch_combine(y_perm, topk_w, inv, T, c->topk, c->hidden, y, s, /*pdl=*/true, err_out);
+  record(dbg, 6, s);
+  return cuda_status(e);
+}
+
+beam_status_t check_nvfp4_weights(const beam_moe_nvfp4_weights_t* w, const beam_moe_config_t* c) {
+  if (w == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (!beam::nvfp4_experts_supported(c->num_experts, c->hidden, c->d_ff)) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  if (!w->q_gate_up || !w->sf_gate_up || !w->q_down || !w->sf_down || !w->expert_scale) return BEAM_ERR_INVALID_ARG;
+  if (!(w->input_scale > 0.0f) || !(w->act_scale > 0.0f) || !std::isfinite(w->input_scale) ||
+      !std::isfinite(w->act_scale))
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(w->q_gate_up) || !aligned16(w->sf_gate_up) || !aligned16(w->q_down) || !aligned16(w->sf_down) ||
+      !aligned4(w->expert_scale))
+    return BEAM_ERR_MISALIGNED;
+  return BEAM_OK;
+}
+
+beam::Nvfp4Experts nvfp4_of(const beam_moe_nvfp4_weights_t* w) {
+  return beam::Nvfp4Experts{w->q_gate_up, w->sf_gate_up, w->q_down, w->sf_down, w->expert_scale};
 }
 
 }  // namespace
@@ -374,15 +449,17 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
                                 const beam_moe_config_t* cfg, uint16_t* h_out, uint16_t* y_out,
                                 const beam_moe_debug_t* dbg, void* ws, size_t ws_bytes, void* stream,
                                 bool route_sync_zeroed, beam_moe_uncombined_t* uncombined = nullptr,
-                                int* err_out = nullptr) {
+                                int* err_out = nullptr, const beam_moe_nvfp4_weights_t* fp4w = nullptr) {
   beam_status_t st = check_config(cfg);
   if (st != BEAM_OK) return st;
   if ((st = check_T(T, cfg)) != BEAM_OK) return st;
   if (n < 1 || wt == nullptr) return BEAM_ERR_INVALID_ARG;
+  const bool fp4 = fp4w != nullptr;  // NVFP4 experts (the bf16 expert weights are then unused)
+  if (fp4 && (st = check_nvfp4_weights(fp4w, cfg)) != BEAM_OK) return st;
   launch_counter() = 0;
   if (T == 0) return BEAM_OK;
   if (!h || !x || !h_out || (y_out == nullptr) == (uncombined == nullptr) || !ws || !wt->w_post || !wt->w_pre ||
-      !wt->router_w || !wt->bias || !wt->w_gate_up || !wt->w_down)
+      !wt->router_w || !wt->bias || (!fp4 && (!wt->w_gate_up || !wt->w_down)) || (fp4 && uncombined))
     return BEAM_ERR_INVALID_ARG;
   if (!aligned16(h) || !aligned16(x) || !aligned16(h_out) || !aligned16(y_out) || !aligned16(wt->w_post) ||
       !aligned16(wt->w_pre) || !aligned16(wt->router_w) || !aligned4(wt->bias) || !aligned16(wt->w_gate_up) ||
@@ -395,8 +472,8 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
     return BEAM_ERR_MISALIGNED;
   DeviceInfo d;
   if ((st = device_info(&d)) != BEAM_OK) return st;
-  if (ws_bytes < layer_ws(cfg, T, d.sms).total) return BEAM_ERR_WORKSPACE_TOO_SMALL;
-  const LayerWs L = layer_ws(cfg, T, d.sms);
+  const LayerWs L = layer_ws(cfg, T, d.sms, fp4);
+  if (ws_bytes < L.total) return BEAM_ERR_WORKSPACE_TOO_SMALL;
   char* base = static_cast<char*>(ws);
   uint16_t* z = (dbg && dbg->z) ? dbg->z : reinterpret_cast<uint16_t*>(base + L.z);
   float* logits = (dbg && dbg->logits) ? dbg->logits : reinterpret_cast<float*>(base + L.logits);
@@ -419,8 +496,9 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
   const bool pdl = true;
   int* router_ticket = reinterpret_cast<int*>(base + L.router_ticket);
   beam::GemmPlan p0, p1;
-  beam::plan_experts(T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms, &p0, &p1);
-  char* gemm_scratch = base + L.experts + experts_ws(cfg, T, d.sms).gemm;
+  beam::plan_experts(T, cfg->topk, cfg->num_experts, cfg->hidden, cfg->d_ff, d.sms, &p0, &p1, fp4);
+  char* gemm_scratch =
+      base + L.experts + (fp4 ? experts_ws_fp4(cfg, T, d.sms).gemm : experts_ws(cfg, T, d.sms).gemm);
   cudaError_t e;
   if (beam::route_decode_supported(T, H, cfg->num_experts, cfg->num_groups, cfg->topk)) {
     // decode sizes: boundary, router, top-k, permutation and the GEMM scratch
@@ -435,9 +513,14 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
     record(dbg, 2, s);
     launches += launch_counter();
     launch_counter() = 0;
-    const int* ready = beam::fused_experts_supported(p0, p1) ? router_ticket + 1 : nullptr;
-    st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
-                     dbg, pdl, /*cleared=*/true, ready, err_out);
+    if (fp4) {
+      st = run_experts_fp4(x_perm, offsets, nvfp4_of(fp4w), fp4w->input_scale, fp4w->act_scale, w, inv, T, cfg,
+                           y_out, base + L.experts, d.sms, s, dbg, pdl, /*cleared=*/true, err_out, nullptr);
+    } else {
+      const int* ready = beam::fused_experts_supported(p0, p1) ? router_ticket + 1 : nullptr;
+      st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms,
+                       s, dbg, pdl, /*cleared=*/true, ready, err_out);
+    }
     launch_counter() += launches;
     return st;
   }
@@ -470,8 +553,12 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
   if (e != cudaSuccess) return BEAM_ERR_CUDA;
   launches += launch_counter();
   launch_counter() = 0;
-  st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
-                   dbg, pdl, /*cleared=*/true, nullptr, err_out);
+  if (fp4)
+    st = run_experts_fp4(x_perm, offsets, nvfp4_of(fp4w), fp4w->input_scale, fp4w->act_scale, w, inv, T, cfg, y_out,
+                         base + L.experts, d.sms, s, dbg, pdl, /*cleared=*/true, err_out, nullptr);
+  else
+    st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms, s,
+                     dbg, pdl, /*cleared=*/true, nullptr, err_out);
   launch_counter() += launches;
   return st;
 }
@@ -509,6 +596,102 @@ beam_status_t beam_boundary_norm_combine(const uint16_t* h, const uint16_t* y_pe
   if (st != BEAM_OK) return st;
   return cuda_status(beam::launch_boundary_combine(h, y_perm, topk_w, inv_perm, K, w_post, w_pre, T, H, eps, n,
                                                    h_out, z_out, static_cast<cudaStream_t>(stream), true));
+}
+
+// ------------------------------------------------------------------ NVFP4 experts
+size_t beam_nvfp4_expert_bytes(const beam_moe_config_t* cfg, size_t* q_gate_up, size_t* sf_gate_up, size_t* q_down,
+                               size_t* sf_down) {
+  if (check_config(cfg) != BEAM_OK || !beam::nvfp4_experts_supported(cfg->num_experts, cfg->hidden, cfg->d_ff))
+    return 0;
+  const size_t E = cfg->num_experts, H = cfg->hidden, F = cfg->d_ff;
+  const size_t a = E * 2 * F * H / 2, b = E * 2 * F * H / 16, c = E * H * F / 2, dd = E * H * F / 16;
+  if (q_gate_up) *q_gate_up = a;
+  if (sf_gate_up) *sf_gate_up = b;
+  if (q_down) *q_down = c;
+  if (sf_down) *sf_down = dd;
+  return a + b + c + dd + E * sizeof(float);
+}
+
+beam_status_t beam_nvfp4_quantize_experts(const uint16_t* w_gate_up, const uint16_t* w_down,
+                                          const beam_moe_config_t* cfg, uint8_t* q_gate_up, uint8_t* sf_gate_up,
+                                          uint8_t* q_down, uint8_t* sf_down, float* expert_scale, void* stream) {
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if (!beam::nvfp4_experts_supported(cfg->num_experts, cfg->hidden, cfg->d_ff)) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  if (!w_gate_up || !w_down || !q_gate_up || !sf_gate_up || !q_down || !sf_down || !expert_scale)
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(q_gate_up) || !aligned16(sf_gate_up) ||
+      !aligned16(q_down) || !aligned16(sf_down) || !aligned4(expert_scale))
+    return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  launch_counter() = 0;
+  return cuda_status(beam::launch_quantize_experts(w_gate_up, w_down, cfg->num_experts, cfg->hidden, cfg->d_ff,
+                                                   q_gate_up, sf_gate_up, q_down, sf_down, expert_scale, d.sms,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+beam_status_t beam_nvfp4_quantize_rows(const uint16_t* x, int rows, int K, float scale, uint8_t* q, uint8_t* sf,
+                                       void* stream) {
+  if (rows < 0 || K <= 0 || !(scale > 0.0f) || !std::isfinite(scale)) return BEAM_ERR_INVALID_ARG;
+  if (K % 64 != 0) return BEAM_ERR_UNSUPPORTED_SHAPE;
+  launch_counter() = 0;
+  if (rows == 0) return BEAM_OK;
+  if (!x || !q || !sf) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BEAM_ERR_MISALIGNED;
+  DeviceInfo d;
+  beam_status_t st = device_info(&d);
+  if (st != BEAM_OK) return st;
+  return cuda_status(beam::launch_quantize_rows(x, rows, K, scale, q, sf, static_cast<cudaStream_t>(stream)));
+}
+
+size_t beam_moe_experts_nvfp4_workspace_size(const beam_moe_config_t* cfg, int T) {
+  if (check_config(cfg) != BEAM_OK || T < 0 ||
+      !beam::nvfp4_experts_supported(cfg->num_experts, cfg->hidden, cfg->d_ff))
+    return 0;
+  return experts_ws_fp4(cfg, T, plan_sms()).total;
+}
+
+beam_status_t beam_moe_experts_nvfp4(const uint16_t* x_perm, const int32_t* expert_offsets,
+                                     const beam_moe_nvfp4_weights_t* weights, const float* topk_w,
+                                     const int32_t* inv_perm, int T, const beam_moe_config_t* cfg, uint16_t* y_out,
+                                     beam_moe_nvfp4_intermediates_t* inter, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  launch_counter() = 0;
+  beam_status_t st = check_config(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_T(T, cfg)) != BEAM_OK) return st;
+  if ((st = check_nvfp4_weights(weights, cfg)) != BEAM_OK) return st;
+  if (inter != nullptr) *inter = beam_moe_nvfp4_intermediates_t{};
+  if (T == 0) return BEAM_OK;
+  if (!x_perm || !expert_offsets || !topk_w || !inv_perm || !y_out || !ws) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(y_out) || !aligned4(expert_offsets) || !aligned4(topk_w) ||
+      !aligned4(inv_perm) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)))
+    return BEAM_ERR_MISALIGNED;
+  if (ws_bytes < beam_moe_experts_nvfp4_workspace_size(cfg, T)) return BEAM_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != BEAM_OK) return st;
+  return run_experts_fp4(x_perm, expert_offsets, nvfp4_of(weights), weights->input_scale, weights->act_scale, topk_w,
+                         inv_perm, T, cfg, y_out, static_cast<char*>(ws), d.sms, static_cast<cudaStream_t>(stream),
+                         nullptr, /*pdl=*/false, /*cleared=*/false, nullptr, inter);
+}
+
+size_t beam_moe_nvfp4_workspace_size(const beam_moe_config_t* cfg, int T) {
+  if (check_config(cfg) != BEAM_OK || T < 0 ||
+      !beam::nvfp4_experts_supported(cfg->num_experts, cfg->hidden, cfg->d_ff))
+    return 0;
+  return layer_ws(cfg, T, plan_sms(), /*fp4=*/true).total;
+}
+
+beam_status_t beam_moe_layer_nvfp4(const uint16_t* h, const uint16_t* x, int n,
+                                   const beam_moe_nvfp4_weights_t* weights, int T, const beam_moe_config_t* cfg,
+                                   uint16_t* h_out, uint16_t* y_out, const beam_moe_debug_t* dbg, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (weights == nullptr) return BEAM_ERR_INVALID_ARG;
+  const beam_moe_weights_t shared = {weights->w_post, weights->w_pre, weights->router_w, weights->bias, nullptr,
+                                     nullptr};
+  return layer_impl(h, x, n, &shared, T, cfg, h_out, y_out, dbg, ws, ws_bytes, stream, false, nullptr, nullptr,
+                    weights);
 }
 
 size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T) {

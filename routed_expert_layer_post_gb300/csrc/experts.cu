@@ -32,6 +32,7 @@
 // on timeout the CTA records a site code in g_device_error and unwinds.
 #include "common.cuh"
 #include "kernels.h"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 #include <cuda.h>
@@ -65,7 +66,14 @@ constexpr int kMaxSplit = 20;                   // largest split-K factor (parti
 struct PhaseParams {
   CUtensorMap tmap_w;   // weights, 3-D: (k, row, plane); expert e owns planes e*planes .. +planes-1
   CUtensorMap tmap_x;   // activations, 2-D: (k, permuted row)
-  uint16_t* out;
+  CUtensorMap tmap_sfx; // NVFP4: activation scale slots, 2-D: (16-byte slot, permuted row)
+  uint16_t* out;        // bf16 output (down; gate/up of the bf16 path)
+  uint8_t* out_q;       // NVFP4 gate/up: codes of the SwiGLU output [rows][F/2]
+  uint8_t* out_sf;      // NVFP4 gate/up: its scale slots [rows][F/64][16]
+  const uint8_t* sfw;   // NVFP4: weight scales, 512-byte atoms [plane][row/128][k-step][4][512]
+  const float* wscale;  // NVFP4: per-expert FP32 weight scales
+  float xscale;         // NVFP4: FP32 scale of the activation operand
+  float out_scale;      // NVFP4 gate/up: FP32 scale of the SwiGLU output it quantizes
   float* partials;      // split-K partial sums of this phase
   int* tickets;         // split-K tickets of this phase (zero before the launch)
   int n_mb;             // 128-row weight blocks per expert
@@ -99,24 +107,38 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int MODE, int BN>
+// FP4 (NVFP4 operands, block-scaled MMAs): a k-step is 256 values, 128 bytes
+// per row as for bf16's 64, so the tile geometry is the same; each stage also
+// holds the weight scales (two 2 KB atom sets) and the activation scales
+// (four 512-byte slot boxes per k-step), copied to tensor memory by the MMA
+// thread (64 columns per stage).
+template <int MODE, int BN, bool FP4 = false>
 struct Cfg {
   static constexpr int kNAcc = MODE == 1 ? 1 : 2;   // accumulators of the widest phase
   static constexpr int kTileBBytes = BN * kBK * 2;
   // MODE 2 keeps a second activation slot so that a down unit can fill a
   // stage with two k-steps (two weight tiles, two activation tiles)
   static constexpr int kBSlots = MODE == 2 ? 2 : 1;
-  static constexpr int kStageBytes = kNAcc * kTileABytes + kBSlots * kTileBBytes;
-  static constexpr int kStagesRaw = (kSmemLimit - 1024 - kCtrlBytes) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kSfABytes = FP4 ? 2 * 2048 : 0;
+  static constexpr int kSfBBytes = FP4 ? kBSlots * 2048 : 0;
+  static constexpr int kSfAOff = kNAcc * kTileABytes + kBSlots * kTileBBytes;
+  static constexpr int kSfBOff = kSfAOff + kSfABytes;
+  static constexpr int kStageBytes = kSfBOff + kSfBBytes;
   static constexpr int kAccCols = kNAcc * BN;
   // two accumulator buffers in TMEM: the epilogue of one tile overlaps the
   // MMAs of the next (four were measured slower at decode)
   static constexpr int kAccBufs = 2;  // one per epilogue group
-  static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols);
+  static constexpr int kSfCols = FP4 ? 64 : 0;  // scale columns per stage: A at +0, B at +32
+  static constexpr int kStagesSmem = (kSmemLimit - 1024 - kCtrlBytes) / kStageBytes;
+  static constexpr int kStagesTmem = FP4 ? (512 - kAccBufs * kAccCols) / 64 : 12;
+  static constexpr int kStagesRaw = kStagesSmem < kStagesTmem ? kStagesSmem : kStagesTmem;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols + kStages * kSfCols);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes;
+  static constexpr int kXStep = FP4 ? 128 : kBK;   // TMA x coordinate of one k-step (bytes or elements)
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
+  static_assert(!FP4 || (MODE == 2 && BN <= 32), "NVFP4 runs the fused launch with token tiles of at most 32");
 };
 
 // Wait until phase `parity` of `bar` has completed. Gives up after `limit_ns`
@@ -241,9 +263,34 @@ __device__ __forceinline__ void store_outputs(const PhaseParams& ph, int rows, i
   }
 }
 
-template <int MODE, int BN>
+// NVFP4 gate/up epilogue for one token column: `val` is this lane's SwiGLU
+// output (column f, the tile's weight row). The 16 lanes of a 16-value group
+// agree on its scale (largest |val| by shuffles) and lane pairs pack two
+// codes per byte. Every lane of the warp calls it, with the same `ok`.
+__device__ __forceinline__ void store_act_fp4(const PhaseParams& ph, float val, bool ok, int row, int f) {
+  float a = ok ? fabsf(val) : 0.f;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFullMask, a, o));
+  float d;
+  const uint32_t s = block_scale(a, ph.out_scale, &d);
+  const uint32_t q = ok ? e2m1_code(val, d) : 0u;
+  const uint32_t hi = __shfl_down_sync(kFullMask, q, 1);
+  if (ok) {
+    const size_t F = static_cast<size_t>(ph.out_ld);
+    if ((f & 1) == 0) ph.out_q[static_cast<size_t>(row) * (F / 2) + (f >> 1)] = static_cast<uint8_t>(q | (hi << 4));
+    if ((f & 15) == 0)
+      ph.out_sf[static_cast<size_t>(row) * (F / 4) + (f >> 6) * 16 + ((f & 63) >> 4)] = static_cast<uint8_t>(s);
+  }
+}
+
+// Index of the 2 KB scale-atom set of (plane, 128-row block, k-step).
+__device__ __forceinline__ size_t sf_atoms(const PhaseParams& ph, int plane, int mb, int k) {
+  return ((static_cast<size_t>(plane) * ph.n_mb + mb) * ph.ksteps + k) * 2048;
+}
+
+template <int MODE, int BN, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<MODE, BN>;
+  using C = Cfg<MODE, BN, FP4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -288,6 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
     if (MODE == 2) {
       ptx::prefetch_tensormap(&p.ph[1].tmap_w);
       ptx::prefetch_tensormap(&p.ph[1].tmap_x);
+    }
+    if (FP4) {
+      ptx::prefetch_tensormap(&p.ph[0].tmap_sfx);
+      ptx::prefetch_tensormap(&p.ph[1].tmap_sfx);
     }
   }
   if (warp == 1) {
@@ -412,6 +463,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       bool dep_ready = (MODE == 0) || (MODE == 2 && p.ready == nullptr);
       int npend = 0;
       int pend_stage[C::kStages], pend_k[C::kStages], pend_row[C::kStages];
+      // the activation tile(s) of one stage (one k-step, or two for `two`),
+      // with NVFP4 also their four 512-byte scale-slot boxes per k-step
+      auto load_b = [&](const PhaseParams& phb, int sidx, int k, int row, bool two) {
+        uint8_t* st = tiles + sidx * C::kStageBytes;
+        ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &phb.tmap_x, &full[sidx], k * C::kXStep, row, pol_x);
+        if (two)
+          ptx::tma_load_2d(st + C::kNAcc * kTileABytes + C::kTileBBytes, &phb.tmap_x, &full[sidx],
+                           (k + 1) * C::kXStep, row, pol_x);
+        if constexpr (FP4) {
+          for (int h = 0; h < (two ? 2 : 1); ++h)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              ptx::tma_load_2d(st + C::kSfBOff + h * 2048 + c * 512, &phb.tmap_sfx, &full[sidx],
+                               (4 * (k + h) + c) * 16, row, pol_x);
+        }
+      };
       auto release_pending = [&]() {
         if (MODE == 1) {
           ptx::griddep_wait();
@@ -420,9 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           if (!wait_counter(p.ready + 1, 1, abort_flag, 10)) ok = false;
           asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
         }
-        for (int i = 0; i < npend; ++i)
-          ptx::tma_load_2d(tiles + pend_stage[i] * C::kStageBytes + C::kNAcc * kTileABytes, &p.ph[0].tmap_x,
-                           &full[pend_stage[i]], pend_k[i] * kBK, pend_row[i], pol_x);
+        for (int i = 0; i < npend; ++i) load_b(p.ph[0], pend_stage[i], pend_k[i], pend_row[i], false);
         npend = 0;
         dep_ready = true;
       };
@@ -436,13 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       auto release_down = [&]() -> bool {
         if (!wait_counter(p.done + pend_gtt, p.ph[0].n_mb, abort_flag, 8)) return false;
         asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
-        for (int i = 0; i < npend; ++i) {
-          uint8_t* st = tiles + pend_stage[i] * C::kStageBytes + C::kNAcc * kTileABytes;
-          ptx::tma_load_2d(st, &p.ph[1].tmap_x, &full[pend_stage[i]], pend_k[i] * kBK, pend_row[i], pol_x);
-          if (pend_two[i])
-            ptx::tma_load_2d(st + C::kTileBBytes, &p.ph[1].tmap_x, &full[pend_stage[i]], (pend_k[i] + 1) * kBK,
-                             pend_row[i], pol_x);
-        }
+        for (int i = 0; i < npend; ++i) load_b(p.ph[1], pend_stage[i], pend_k[i], pend_row[i], pend_two[i]);
         npend = 0;
         ready_gtt = pend_gtt;
         return true;
@@ -480,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
         const int nacc = kind == 0 ? 2 : 1;
-        const uint32_t stage_bytes = nacc * kTileABytes + C::kTileBBytes;
+        const uint32_t stage_bytes = nacc * kTileABytes + C::kTileBBytes + (FP4 ? nacc * 2048 + 2048 : 0);
         const int k0 = w.s * ph.ksteps / ph.split, k1 = (w.s + 1) * ph.ksteps / ph.split;
         const int row0 = s_off[w.e] + w.tt * BN;
         bool defer = false;
@@ -525,11 +584,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           uint8_t* st = tiles + stage * C::kStageBytes;
           if (kps == 2) {
             const bool two = k + 1 < k1;
-            ptx::mbar_arrive_expect_tx(&full[stage], (two ? 2u : 1u) * (kTileABytes + C::kTileBBytes));
-            ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e * ph.planes, pol_w);
+            ptx::mbar_arrive_expect_tx(&full[stage],
+                                       (two ? 2u : 1u) * (kTileABytes + C::kTileBBytes + (FP4 ? 4096u : 0u)));
+            ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * C::kXStep, w.mb * kBM, w.e * ph.planes, pol_w);
             if (two)
-              ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], (k + 1) * kBK, w.mb * kBM,
+              ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], (k + 1) * C::kXStep, w.mb * kBM,
                                w.e * ph.planes, pol_w);
+            if constexpr (FP4) {
+              for (int h = 0; h < (two ? 2 : 1); ++h)
+                ptx::bulk_load(st + C::kSfAOff + h * 2048, ph.sfw + sf_atoms(ph, w.e * ph.planes, w.mb, k + h), 2048,
+                               &full[stage], pol_w);
+            }
             if (defer) {
               pend_stage[npend] = stage;
               pend_k[npend] = k;
@@ -537,10 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               pend_two[npend] = two;
               ++npend;
             } else {
-              ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &ph.tmap_x, &full[stage], k * kBK, row0, pol_x);
-              if (two)
-                ptx::tma_load_2d(st + C::kNAcc * kTileABytes + C::kTileBBytes, &ph.tmap_x, &full[stage],
-                                 (k + 1) * kBK, row0, pol_x);
+              load_b(ph, stage, k, row0, two);
             }
             ++issued;
             if (++stage == C::kStages) {
@@ -550,12 +612,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
             continue;
           }
           ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
-          ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e * ph.planes, pol_w);
+          ptx::tma_load_3d(st, &ph.tmap_w, &full[stage], k * C::kXStep, w.mb * kBM, w.e * ph.planes, pol_w);
           if (kind == 0)  // the up rows: the expert's second plane
-            ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], k * kBK, w.mb * kBM, w.e * ph.planes + 1,
-                             pol_w);
+            ptx::tma_load_3d(st + kTileABytes, &ph.tmap_w, &full[stage], k * C::kXStep, w.mb * kBM,
+                             w.e * ph.planes + 1, pol_w);
+          if constexpr (FP4) {
+            for (int a = 0; a < nacc; ++a)
+              ptx::bulk_load(st + C::kSfAOff + a * 2048, ph.sfw + sf_atoms(ph, w.e * ph.planes + a, w.mb, k), 2048,
+                             &full[stage], pol_w);
+          }
           if (dep_ready) {
-            ptx::tma_load_2d(st + C::kNAcc * kTileABytes, &ph.tmap_x, &full[stage], k * kBK, row0, pol_x);
+            load_b(ph, stage, k, row0, false);
           } else {
             pend_stage[npend] = stage;
             pend_k[npend] = k;
@@ -580,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, BN);
+      constexpr uint32_t idesc = FP4 ? ptx::idesc_nvf4(kBM, BN) : ptx::idesc_bf16_f32(kBM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -609,15 +676,33 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_u32(tiles + stage * C::kStageBytes);
           const uint32_t sb = sa + C::kNAcc * kTileABytes;
+          const int nk = (kps == 2 && k + 1 < k1) ? 2 : 1;  // k-steps in this stage
+          // NVFP4: the stage's scales into its tensor-memory columns (A sets at
+          // +0: per plane, or per k-step for down; B sets at +32: per k-step),
+          // 4 columns per 64-value chunk, before the MMAs that read them
+          const uint32_t sf = tmem_base + static_cast<uint32_t>(C::kAccBufs * C::kAccCols + stage * C::kSfCols);
+          if constexpr (FP4) {
+            const int na = kps == 2 ? nk : nacc;
+            for (int i = 0; i < na; ++i)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) ptx::tmem_cp_32x128_x4(sf + (i * 4 + c) * 4, sa + C::kSfAOff + i * 2048 + c * 512);
+            for (int h = 0; h < nk; ++h)
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                ptx::tmem_cp_32x128_x4(sf + 32 + (h * 4 + c) * 4, sa + C::kSfBOff + h * 2048 + c * 512);
+          }
           if (kps == 2) {
             // two k-steps of one accumulator: (A0, B0) then (A1, B1)
-            const int nk = (k + 1 < k1) ? 2 : 1;
             for (int h = 0; h < nk; ++h) {
 #pragma unroll
               for (int j = 0; j < kBK / 16; ++j) {
                 const uint64_t bdesc = ptx::smem_desc_k128(sb + h * C::kTileBBytes + j * 32);
                 const uint64_t adesc = ptx::smem_desc_k128(sa + h * kTileABytes + j * 32);
-                ptx::mma_bf16(d, adesc, bdesc, idesc, (k > k0 || h > 0 || j > 0) ? 1u : 0u);
+                const uint32_t accum = (k > k0 || h > 0 || j > 0) ? 1u : 0u;
+                if constexpr (FP4)
+                  ptx::mma_nvf4(d, adesc, bdesc, idesc, sf + (h * 4 + j) * 4, sf + 32 + (h * 4 + j) * 4, accum);
+                else
+                  ptx::mma_bf16(d, adesc, bdesc, idesc, accum);
               }
             }
           } else {
@@ -628,7 +713,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               for (int a = 0; a < C::kNAcc; ++a) {
                 if (a < nacc) {
                   const uint64_t adesc = ptx::smem_desc_k128(sa + a * kTileABytes + j * 32);
-                  ptx::mma_bf16(d + a * BN, adesc, bdesc, idesc, (k > k0 || j > 0) ? 1u : 0u);
+                  const uint32_t accum = (k > k0 || j > 0) ? 1u : 0u;
+                  if constexpr (FP4)
+                    ptx::mma_nvf4(d + a * BN, adesc, bdesc, idesc, sf + (a * 4 + j) * 4, sf + 32 + j * 4, accum);
+                  else
+                    ptx::mma_bf16(d + a * BN, adesc, bdesc, idesc, accum);
                 }
               }
             }
@@ -686,6 +775,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       const int valid = min(BN, s_off[w.e + 1] - row0);
       const int col = w.mb * kBM + m;
       const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * C::kAccCols);
+      // NVFP4: the MMA sums products of block-scaled values; the two FP32
+      // scales (the expert's and the activation's) multiply the sum
+      const float gs = FP4 ? __fmul_rn(ph.wscale[w.e], ph.xscale) : 1.0f;
       bool tile_done = false;  // this unit completed its tile's outputs
       bool released = false;   // the accumulator was already handed back
       if (ph.split == 1) {
@@ -700,6 +792,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           for (int a = 0; a < 2; ++a)
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[a][j] = (a < C::kNAcc && a < nacc) ? __uint_as_float(r[a][j]) : 0.f;
+          if constexpr (FP4) {
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[a][j] = __fmul_rn(v[a][j], gs);
+            if (kind == 0) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float g = v[0][j];
+                store_act_fp4(ph, g / (1.0f + __expf(-g)) * v[1][j], c0 + j < valid, row0 + c0 + j, col);
+              }
+              continue;
+            }
+          }
           store_outputs<BN>(ph, p.rows, kind, v, c0, valid, row0, col);
         }
         tile_done = true;
@@ -764,6 +870,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               }
             }
             const int row = row0 + j;
+            if constexpr (FP4) {
+              g = __fmul_rn(g, gs);
+              u2 = __fmul_rn(u2, gs);
+              if (kind == 0) {  // every lane of the group runs this column: the scale is shared
+                store_act_fp4(ph, g / (1.0f + __expf(-g)) * u2, true, row, col);
+                continue;
+              }
+            }
             if (row >= 0 && row < p.rows && col < ph.out_ld) {
               const float val = kind == 0 ? g / (1.0f + __expf(-g)) * u2 : g;
               ph.out[static_cast<size_t>(row) * ph.out_ld + col] = static_cast<uint16_t>(f2bf(val));
@@ -1036,29 +1150,29 @@ EncodeFn get_encode_fn() {
 }
 
 bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                const cuuint32_t* box) {
+                const cuuint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, bool FP4 = false>
 cudaError_t launch_mode_bn(const GemmParams& prm, int grid, cudaStream_t stream, bool pdl) {
-  using C = Cfg<MODE, BN>;
+  using C = Cfg<MODE, BN, FP4>;
   static std::once_flag once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const cudaError_t err =
-      launch_kernel(moe_gemm_kernel<MODE, BN>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, prm);
+      launch_kernel(moe_gemm_kernel<MODE, BN, FP4>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, prm);
   ++launch_counter();
   return err;
 }
@@ -1089,19 +1203,22 @@ int accum_cols(int mode, int bn) { return (mode == 0 ? 2 : 1) * bn; }
 
 }  // namespace
 
-GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int units_per_sm) {
+GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int units_per_sm, bool fp4) {
   GemmPlan plan{};
   const long long entries = static_cast<long long>(T) * K;
   const long long touched = entries < E ? entries : E;
   const double r = touched > 0 ? static_cast<double>(entries) / static_cast<double>(touched) : 1.0;
   // token tile: the smallest width holding the mean rows per expert with some
   // slack; up to 128 for gate/up (two accumulators) and 256 for down, where
-  // the wider tile halves the operand bytes per MMA at prefill sizes
-  const int bn_max = mode == 0 ? 128 : 256;
+  // the wider tile halves the operand bytes per MMA at prefill sizes (NVFP4:
+  // up to 32, the rows one lane quarter holds the activation scales of)
+  const int bn_max = fp4 ? 32 : (mode == 0 ? 128 : 256);
   int bn = 16;
   while (bn < bn_max && 1.25 * r > bn) bn <<= 1;
   const int n_mb = mode == 0 ? (F + kBM - 1) / kBM : H / kBM;
-  const int ksteps = mode == 0 ? H / kBK : F / kBK;
+  // a k-step is 128 bytes of each weight row: 64 bf16 or 256 NVFP4 values
+  const int kstep = fp4 ? 256 : kBK;
+  const int ksteps = mode == 0 ? H / kstep : F / kstep;
   plan.bn = bn;
   plan.max_token_tiles = static_cast<int>(touched + entries / bn);
   plan.max_tiles = plan.max_token_tiles * n_mb;
@@ -1111,11 +1228,14 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int
   // last units are: when tiles are few (decode), split the reduction until
   // there are at least `units_per_sm` units per SM, keeping at least 128 KB
   // of weights per unit (4 k-steps of gate+up rows, 8 of down rows) so that
-  // the per-unit epilogue stays hidden behind the next unit's loads.
+  // the per-unit epilogue stays hidden behind the next unit's loads. Only
+  // narrow token tiles (<= 64) are split: the final sum of a split tile
+  // walks its columns one at a time, which costs more than the balance gains
+  // once a tile holds 128 or 256 columns (few experts with many rows each).
   const int min_ksteps = mode == 0 ? 4 : 8;
   int split = 1;
   const long long target = static_cast<long long>(units_per_sm) * num_sms;
-  if (est < target) {
+  if (est < target && bn <= 64) {
     for (int s = 2; s <= ksteps && s <= kMaxSplit; ++s) {
       if (ksteps % s != 0) continue;
       if (ksteps / s < min_ksteps) break;
@@ -1199,6 +1319,51 @@ cudaError_t launch_fused_bn(const GemmParams& prm, int grid, cudaStream_t stream
   return launch_mode_bn<2, BN>(prm, grid, stream, pdl);
 }
 
+// One NVFP4 phase: codes read as bytes (two values each), 128-byte k-steps
+// (256 values) with the 128-byte swizzle; activation scale slots as 16-byte
+// x 32-row boxes without swizzle.
+bool fill_phase_fp4(PhaseParams& ph, int mode, const GemmPlan& plan, const uint8_t* wq, const uint8_t* wsf,
+                    const float* wscale, const uint8_t* xq, const uint8_t* xsf, float xscale, int rows, int E, int H,
+                    int F, char* base, const ScratchLayout& l) {
+  const int kdim = mode == 0 ? H : F;
+  const int planes = mode == 0 ? 2 : 1;
+  const int prows = mode == 0 ? F : H;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim / 2), static_cast<cuuint64_t>(prows),
+                                static_cast<cuuint64_t>(E) * planes};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kdim / 2),
+                                   static_cast<cuuint64_t>(kdim / 2) * static_cast<cuuint64_t>(prows)};
+    const cuuint32_t box[3] = {128, kBM, 1};
+    if (!encode_map(&ph.tmap_w, wq, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) return false;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kdim / 2), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim / 2)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(plan.bn)};
+    if (!encode_map(&ph.tmap_x, xq, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) return false;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kdim / 4), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim / 4)};
+    const cuuint32_t box[2] = {16, 32};
+    if (!encode_map(&ph.tmap_sfx, xsf, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+      return false;
+  }
+  ph.sfw = wsf;
+  ph.wscale = wscale;
+  ph.xscale = xscale;
+  ph.tickets = reinterpret_cast<int*>(base + (mode == 0 ? l.tickets0 : l.tickets1));
+  ph.partials = plan.split > 1 ? reinterpret_cast<float*>(base + (mode == 0 ? l.partials0 : l.partials1)) : nullptr;
+  ph.n_mb = prows / kBM;
+  ph.ksteps = kdim / 256;
+  ph.split = plan.split;
+  ph.out_ld = mode == 0 ? F : H;
+  ph.planes = planes;
+  ph.max_tiles = plan.max_tiles;
+  return true;
+}
+
 }  // namespace
 
 size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down) {
@@ -1232,14 +1397,14 @@ cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down,
                    : launch_mode<1>(plan.bn, prm, num_sms, stream, pdl);
 }
 
-void plan_experts(int T, int K, int E, int H, int F, int num_sms, GemmPlan* gate_up, GemmPlan* down) {
-  *gate_up = plan_gemm(0, T, K, E, H, F, num_sms);
-  *down = plan_gemm(1, T, K, E, H, F, num_sms);
+void plan_experts(int T, int K, int E, int H, int F, int num_sms, GemmPlan* gate_up, GemmPlan* down, bool fp4) {
+  *gate_up = plan_gemm(0, T, K, E, H, F, num_sms, 16, fp4);
+  *down = plan_gemm(1, T, K, E, H, F, num_sms, 16, fp4);
   if (fused_experts_supported(*gate_up, *down)) {
     // One launch runs both phases from one unit list, so only the down units
     // at its end need to be small for balance; fewer, larger gate/up units
     // mean fewer split-K tickets, whose round trips the epilogue waits on.
-    *gate_up = plan_gemm(0, T, K, E, H, F, num_sms, 4);
+    *gate_up = plan_gemm(0, T, K, E, H, F, num_sms, 4, fp4);
   }
 }
 
@@ -1270,6 +1435,35 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
     case 32: return launch_fused_bn<32>(prm, num_sms, stream, pdl);
     default: return launch_fused_bn<64>(prm, num_sms, stream, pdl);
   }
+}
+
+cudaError_t launch_fused_experts_fp4(const GemmPlan& gate_up, const GemmPlan& down, const Nvfp4Experts& wt,
+                                     const uint8_t* xq, const uint8_t* xsf, float x_scale, const int32_t* offsets,
+                                     int rows, int E, int H, int F, uint8_t* act_q, uint8_t* act_sf, float act_scale,
+                                     uint16_t* y_perm, void* scratch, int num_sms, cudaStream_t stream, bool pdl) {
+  if (!fused_experts_supported(gate_up, down) || gate_up.bn > 32) return cudaErrorInvalidValue;
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  char* base = static_cast<char*>(scratch);
+  const ScratchLayout l = scratch_layout(gate_up, down);
+  if (!fill_phase_fp4(prm.ph[0], 0, gate_up, wt.q_gate_up, wt.sf_gate_up, wt.scale, xq, xsf, x_scale, rows, E, H, F,
+                      base, l) ||
+      !fill_phase_fp4(prm.ph[1], 1, down, wt.q_down, wt.sf_down, wt.scale, act_q, act_sf, act_scale, rows, E, H, F,
+                      base, l))
+    return cudaErrorInvalidValue;
+  prm.ph[0].out_q = act_q;
+  prm.ph[0].out_sf = act_sf;
+  prm.ph[0].out_scale = act_scale;
+  prm.ph[1].out = y_perm;
+  prm.offsets = offsets;
+  prm.counter = reinterpret_cast<int*>(base) + 2;
+  prm.done = reinterpret_cast<int*>(base + l.done);
+  prm.E = E;
+  prm.rows = rows;
+  prm.max_token_tiles = gate_up.max_token_tiles;
+  prm.ready = nullptr;
+  return gate_up.bn == 16 ? launch_mode_bn<2, 16, true>(prm, num_sms, stream, pdl)
+                          : launch_mode_bn<2, 32, true>(prm, num_sms, stream, pdl);
 }
 
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,

@@ -79,11 +79,14 @@ struct GemmPlan {
   int max_token_tiles;  // upper bound on (expert, token-tile) pairs
   int max_tiles;        // upper bound on (expert, row-block, token-tile) tiles
 };
-// mode 0: gate/up + SwiGLU (weight rows 2F, reduction H); mode 1: down (rows H, reduction F)
-GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int units_per_sm = 16);
+// mode 0: gate/up + SwiGLU (weight rows 2F, reduction H); mode 1: down (rows H, reduction F).
+// `fp4`: NVFP4 operands (256-value k-steps, token tiles of at most 32).
+GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int units_per_sm = 16,
+                   bool fp4 = false);
 // The plans of a gate/up + down pass as run by the experts stage (the fused
 // launch when fused_experts_supported, else two launches).
-void plan_experts(int T, int K, int E, int H, int F, int num_sms, GemmPlan* gate_up, GemmPlan* down);
+void plan_experts(int T, int K, int E, int H, int F, int num_sms, GemmPlan* gate_up, GemmPlan* down,
+                  bool fp4 = false);
 // Scratch shared by one gate/up + down pass (unit counters, split-K tickets
 // and partial sums); it must be cleared with clear_gemm_scratch before the
 // gate/up GEMM (one memset; each GEMM leaves its tickets at zero).
@@ -103,6 +106,30 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl = false);
+// ---- NVFP4 experts (nvfp4.cu, experts.cu)
+// Expert weights as E2M1 codes (two per byte), E4M3 scales per 16 values in
+// 512-byte atoms, and one FP32 scale per expert (layouts in beam.h).
+struct Nvfp4Experts {
+  const uint8_t* q_gate_up;   // [E][2F][H/2]
+  const uint8_t* sf_gate_up;  // [2E][F/128][H/256][4][512]
+  const uint8_t* q_down;      // [E][H][F/2]
+  const uint8_t* sf_down;     // [E][H/128][F/256][4][512]
+  const float* scale;         // [E]
+};
+bool nvfp4_experts_supported(int E, int H, int F);
+cudaError_t launch_quantize_experts(const uint16_t* w_gu, const uint16_t* w_d, int E, int H, int F, uint8_t* q_gu,
+                                    uint8_t* sf_gu, uint8_t* q_d, uint8_t* sf_d, float* expert_scale, int num_sms,
+                                    cudaStream_t stream);
+// rows x K bf16 -> codes [rows][K/2] and scale slots [rows][K/64][16] (K % 64 == 0)
+cudaError_t launch_quantize_rows(const uint16_t* x, int rows, int K, float g, uint8_t* q, uint8_t* sf,
+                                 cudaStream_t stream, bool pdl = false);
+// Both NVFP4 GEMMs in one persistent launch (plans from plan_experts with
+// fp4, token tiles <= 32): gate/up + SwiGLU writes the SwiGLU output as
+// NVFP4 (act_q, act_sf, FP32 scale act_scale); down writes bf16 y_perm.
+cudaError_t launch_fused_experts_fp4(const GemmPlan& gate_up, const GemmPlan& down, const Nvfp4Experts& wt,
+                                     const uint8_t* xq, const uint8_t* xsf, float x_scale, const int32_t* offsets,
+                                     int rows, int E, int H, int F, uint8_t* act_q, uint8_t* act_sf, float act_scale,
+                                     uint16_t* y_perm, void* scratch, int num_sms, cudaStream_t stream, bool pdl);
 // `err_out` (optional, device-visible): receives the device error word once
 // the expert launch before the combine has completed.
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,

@@ -131,6 +131,55 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor without swizzle, K-major: core matrices of
+// 8 rows x 16 bytes stored contiguously, `sbo` bytes between 8-row groups
+// along M/N, `lbo` bytes between core matrices along K (not used when the
+// matrix is one 16-byte column wide).
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+
+// Instruction descriptor, kind::mxf4nvf4 with block scaling: A and B E2M1
+// (format 1 at bits 7-9 and 10-12), both K-major, N >> 3 at bits 17-22, E4M3
+// scales (bit 23 = 0), M >> 4 at bits 24-28, scale-factor ids 0, K = 64.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T over K = 64 E2M1 values,
+// one E4M3 scale per 16 (scale_vec::4X). SFA for row m: lane m, column
+// sfa + m/32, byte j = group j; SFB for row n: lane 32p + n%32 of every
+// subpartition p, column sfb + n/32. Both scale addresses 4-column aligned.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// 32 rows x 16 bytes from shared memory (plain layout, rows 16 bytes apart)
+// to tensor-memory columns taddr .. taddr+3, row i in lane i of each of the
+// four 32-lane subpartitions.
+__device__ __forceinline__ void tmem_cp_32x128_x4(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(smem_desc_plain(saddr, 4096, 128))
+               : "memory");
+}
+
+// Contiguous copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {

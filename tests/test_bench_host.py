@@ -61,12 +61,18 @@ def test_clock_summary_parsing():
 def test_defaults_and_peaks():
     a = bench.parse_args([])
     assert a.config == "all" and a.warmup >= 3 and a.impl == "ours"
-    names, head = bench.workloads(a)
-    assert names == ["toy", "decode_t1", "decode_t64", "prefill_t2048", "prefill_t16384"]
-    assert head == "prefill_t16384"
+    runs, head = bench.workloads(a)
+    names = ["toy", "decode_t1", "decode_t64", "prefill_t2048", "prefill_t16384"]
+    assert runs == [(n, False) for n in names] + [("decode_t1", True), ("decode_t64", True)]
+    assert head == ("prefill_t16384", False)
+    assert [bench.run_key(r) for r in runs[-2:]] == ["decode_t1_nvfp4", "decode_t64_nvfp4"]
     assert all(bench.steps_for(a, n) > 0 and bench.batches_for(a, n) > 0 for n in names)
+    assert bench.workloads(bench.parse_args(["--no-nvfp4"]))[0] == [(n, False) for n in names]
     one = bench.parse_args(["--config", "decode_t1", "--steps", "7"])
-    assert bench.workloads(one) == (["decode_t1"], "decode_t1") and bench.steps_for(one, "decode_t1") == 7
+    assert bench.workloads(one) == ([("decode_t1", False)], ("decode_t1", False))
+    assert bench.steps_for(one, "decode_t1") == 7
+    fp4 = bench.parse_args(["--config", "decode_t64", "--nvfp4"])
+    assert bench.workloads(fp4) == ([("decode_t64", True)], ("decode_t64", True))
     with pytest.raises(SystemExit):
         bench.parse_args(["--tokens", "8"])  # overrides need a single workload
     peaks, kind = bench.load_peaks()
