@@ -36,6 +36,7 @@
 #include "ptx.cuh"
 
 #include <cuda.h>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -912,6 +913,302 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   if (MODE == 2 && p.ready != nullptr) ptx::griddep_wait();
 }
 
+// ------------------------------------------------------------------ paired-SM GEMMs (prefill)
+// At prefill sizes the expert GEMMs are tensor-core bound, and what holds the
+// tensor pipe below its peak is how much MMA work the shared-memory ring
+// covers while its loads are in flight (four 48 KB stages per SM above). A
+// pair of CTAs on two SMs (a cluster of two) issues tcgen05.mma with
+// cta_group::2: one M = 256, N = 256 MMA per 16-value slice, each CTA holding
+// 128 rows of the weight operand and 128 of the 256 token rows, each CTA's
+// tensor memory receiving its own 128 weight rows of the product (all 256
+// tokens). A stage is then 32 KB per SM (16 KB of weights, 16 KB of tokens)
+// for the same MMA work per SM, so six stages fit. Both CTAs' loads of a stage
+// complete on the leader's barrier (TMA with .cta_group::2), which expects the
+// pair's bytes, so the leader issues a stage's MMAs with no extra hop.
+//
+// Gate/up: a CTA's 128 weight rows are 64 gate rows and the up rows of the
+// same 64 d_ff columns (two 64-row TMA boxes), so its accumulator holds gate
+// in tensor-memory lanes 0-63 and up in lanes 64-127; the epilogue pairs them
+// through shared memory for SwiGLU. A pair covers 128 d_ff columns. Down: 128
+// rows of W_d per CTA, 256 per pair.
+//
+// Work: a static round-robin over tiles (expert, weight row block, 256-token
+// tile), both CTAs of a pair walking the same sequence (tiles are equal work,
+// and no tile waits on another). Roles (320 threads): warp 0 loads this CTA's
+// halves; warp 1 of the leader CTA (cluster rank 0) issues the MMAs of a stage
+// once both halves have landed and commits to both CTAs' barriers; warps 2-9
+// are two epilogue groups taking alternate tiles, each CTA reading its own
+// rows (the peer's groups release the accumulator with a remote arrive).
+constexpr int kPairN = 256;                                        // tokens per tile
+constexpr int kPairRows = 128;                                     // token rows per CTA
+constexpr int kPairStageBytes = kTileABytes + kPairRows * kBK * 2;  // 32 KB
+constexpr int kPairXchBytes = 2 * 64 * 16 * 4;                     // SwiGLU exchange, both groups
+constexpr int kPairStages = (kSmemLimit - 1024 - kCtrlBytes - kPairXchBytes) / kPairStageBytes;
+constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + kPairXchBytes + kCtrlBytes;
+constexpr int kPairTmemCols = 2 * kPairN;                          // two accumulator buffers
+static_assert(kPairStages >= 6, "six 32 KB stages per SM");
+
+// Bounded wait at cluster scope (for barriers the other CTA arrives on).
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int site) {
+  const uint32_t addr = ptx::smem_u32(bar);
+  if (ptx::mbar_try_wait_cluster(addr, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait_cluster(addr, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        if (abort_flag != nullptr) *abort_flag = 1;
+        atomicCAS(&g_device_error, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+// MODE 0: gate/up + SwiGLU (ph[0], planes of F rows, tensor map box 64 rows);
+// MODE 1: down (ph[0], one plane of H rows, box 128 rows).
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    moe_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* xch = reinterpret_cast<float*>(tiles + kPairStages * kPairStageBytes);  // [group][16 columns][64 lanes]
+  uint8_t* ctrl = tiles + kPairStages * kPairStageBytes + kPairXchBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + kPairStages;
+  uint64_t* tfull = empty + kPairStages;
+  uint64_t* tempty = tfull + 2;           // leader: both CTAs' epilogues released the accumulator
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_off = s_flags + 8;
+  int* s_ntt = s_off + kMaxE + 1;
+  int* s_ttstart = s_ntt + kMaxE;
+  volatile int* abort_flag = s_flags;
+  const PhaseParams& ph = p.ph[0];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = ptx::cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
+  if (tid == 0) {
+    for (int i = 0; i < kPairStages; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 2);
+    }
+    ptx::mbar_init(drain, 1);
+    for (int i = 0; i < 8; ++i) s_flags[i] = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&ph.tmap_w);
+    ptx::prefetch_tensormap(&ph.tmap_x);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_slot, kPairTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::griddep_wait();  // offsets and activation rows come from the previous kernels
+  ptx::griddep_launch_dependents();
+  for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
+  __syncthreads();
+  if (warp == 0) {
+    const int per_lane = (p.E + 31) / 32;
+    int local = 0;
+    for (int j = 0; j < per_lane; ++j) {
+      const int e = lane * per_lane + j;
+      if (e < p.E) {
+        const int ntt = (max(0, s_off[e + 1] - s_off[e]) + kPairN - 1) / kPairN;
+        s_ntt[e] = ntt;
+        local += ntt;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per_lane; ++j) {
+      const int e = lane * per_lane + j;
+      if (e < p.E) {
+        s_ttstart[e] = run;
+        run += s_ntt[e];
+      }
+    }
+    if (lane == 31) s_ttstart[p.E] = incl;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_units = s_ttstart[p.E] * ph.n_mb;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (this CTA's halves)
+    if (lane == 0) {
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      // both CTAs' loads complete on the leader's full barrier, which expects the pair's bytes
+      const uint32_t full0 = ptx::cluster_addr(full, 0);
+      for (int u = pair; u < n_units && ok; u += npairs) {
+        const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
+        const int row0 = s_off[w.e] + w.tt * kPairN + static_cast<int>(rank) * kPairRows;
+        for (int k = 0; k < ph.ksteps; ++k) {
+          if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, 31, kTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = tiles + stage * kPairStageBytes;
+          const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+          if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kPairStageBytes);
+          if (MODE == 0) {
+            const int f0 = w.mb * kBM + static_cast<int>(rank) * 64;
+            ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, f0, 2 * w.e, pol_w);                    // gate rows
+            ptx::tma_load_3d_pair(st + kTileABytes / 2, &ph.tmap_w, fb, k * kBK, f0, 2 * w.e + 1, pol_w);  // up
+          } else {
+            ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, w.mb * 2 * kBM + static_cast<int>(rank) * kBM, w.e,
+                                  pol_w);
+          }
+          ptx::tma_load_2d_pair(st + kTileABytes, &ph.tmap_x, fb, k * kBK, row0, pol_x);
+          ++issued;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // unwinding: let the copies already in flight land (the peer's land on these barriers too)
+        for (int i = 0; i < kPairStages && i < issued; ++i) {
+          const uint32_t par = (i < stage) ? phase : (phase ^ 1u);
+          wait_bar(&full[i], par, nullptr, 32, kDrainNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader CTA only)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      if (leader) {
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kPairN);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = pair; u < n_units && ok; u += npairs) {
+          if (!wait_bar_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, 33)) break;
+          ptx::tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
+          for (int k = 0; k < ph.ksteps; ++k) {
+            if (!wait_bar_cluster(&full[stage], phase, abort_flag, 34)) {  // both halves landed
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = ptx::smem_u32(tiles + stage * kPairStageBytes);
+            const uint32_t sb = sa + kTileABytes;
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j)
+              ptx::mma_bf16_pair(d, ptx::smem_desc_k128(sa + j * 32), ptx::smem_desc_k128(sb + j * 32), idesc,
+                                 (k > 0 || j > 0) ? 1u : 0u);
+            ptx::mma_commit_pair(&empty[stage]);
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit_pair(&tfull[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+        ptx::mma_commit_pair(drain);  // every MMA of the pair issued here has completed once `drain` flips
+        wait_bar(drain, 0, nullptr, 36, kTimeoutNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue groups (warps 2-5, 6-9)
+    const int eg = (warp - 2) >> 2;
+    const int sub = warp & 3;  // TMEM lane quarter
+    const int m = sub * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+    const uint32_t bar_id = 1 + eg;
+    float* x = xch + eg * 64 * 16;
+    const uint32_t tempty_leader = ptx::cluster_addr(&tempty[eg], 0);
+    uint32_t acc_phase = 0;
+    for (int i = eg;; i += 2) {
+      const int u = pair + i * npairs;
+      if (u >= n_units) break;
+      if (!wait_bar(&tfull[eg], acc_phase, abort_flag, 38, kTimeoutNs)) break;
+      ptx::tc_fence_after();
+      const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
+      const int row0 = s_off[w.e] + w.tt * kPairN;
+      const int valid = min(kPairN, s_off[w.e + 1] - row0);
+      const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(eg * kPairN);
+      for (int c0 = 0; c0 < valid; c0 += 16) {
+        uint32_t r[16];
+        ptx::tmem_ld16(tb + c0, r);
+        ptx::tmem_ld_wait();
+        if (MODE == 1) {
+          const int col = w.mb * 2 * kBM + static_cast<int>(rank) * kBM + m;  // row of W_d = output column
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < valid)
+              ph.out[static_cast<size_t>(row0 + c0 + j) * ph.out_ld + col] =
+                  static_cast<uint16_t>(f2bf(__uint_as_float(r[j])));
+        } else {
+          if (m >= 64) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j * 64 + (m - 64)] = __uint_as_float(r[j]);
+          }
+          ptx::named_bar_sync(bar_id, 128);
+          if (m < 64) {
+            const int col = w.mb * kBM + static_cast<int>(rank) * 64 + m;  // d_ff column
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < valid) {
+                const float g = __uint_as_float(r[j]);
+                const float val = g / (1.0f + __expf(-g)) * x[j * 64 + m];
+                ph.out[static_cast<size_t>(row0 + c0 + j) * ph.out_ld + col] = static_cast<uint16_t>(f2bf(val));
+              }
+            }
+          }
+          ptx::named_bar_sync(bar_id, 128);  // the exchange buffer is free again
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::named_bar_sync(bar_id, 128);
+      if (warp == 2 + 4 * eg && lane == 0) {
+        if (leader) ptx::mbar_arrive(&tempty[eg]);
+        else ptx::mbar_arrive_remote(tempty_leader);
+      }
+      acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the leader's MMAs into the peer's tensor memory are done before either frees it
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kPairTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------ combine
 // y[t] = bf16(sum_k w[t][k] * y_perm[inv_perm[t*K+k]]), k in slot order, one
 // thread per 8 hidden columns of a token; no atomics. KMAX bounds K: the
@@ -1244,6 +1541,13 @@ GemmPlan plan_gemm(int mode, int T, int K, int E, int H, int F, int num_sms, int
     }
   }
   plan.split = split;
+  // prefill sizes: paired-SM tiles of 256 tokens once the mean rows per
+  // expert fill them (the tensor-core-bound regime); no split then
+  plan.pair = !fp4 && split == 1 && r >= 192.0 && H % (2 * kBM) == 0 && F % kBM == 0;
+  if (plan.pair) {
+    plan.max_token_tiles = static_cast<int>(touched + entries / kPairN);
+    plan.max_tiles = plan.max_token_tiles * (mode == 0 ? F / kBM : H / (2 * kBM));
+  }
   return plan;
 }
 
@@ -1366,6 +1670,79 @@ bool fill_phase_fp4(PhaseParams& ph, int mode, const GemmPlan& plan, const uint8
 
 }  // namespace
 
+namespace {
+
+// The pairs launched: as many clusters of two as can be resident at once
+// (GPCs with an odd number of free SMs leave one idle), so that no pair
+// waits for a second wave; queried once per device.
+template <int MODE>
+cudaError_t launch_pair_mode(const GemmParams& prm, int num_sms, cudaStream_t stream, bool pdl) {
+  static std::once_flag once[64];
+  static int pairs[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(moe_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kPairSmem);
+    int clusters = 0;
+    if (attr_err == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((num_sms / 2) * 2);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kPairSmem;
+      if (cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        clusters = 0;
+      }
+    }
+    pairs[dev & 63] = clusters > 0 ? std::min(clusters, num_sms / 2) : num_sms / 2;
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const cudaError_t err = launch_kernel(moe_gemm_pair_kernel<MODE>, dim3(2 * pairs[dev & 63]), dim3(kThreads),
+                                        kPairSmem, stream, pdl, prm);
+  ++launch_counter();
+  return err;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* act_in, const int32_t* offsets,
+                             int rows, int E, int H, int F, uint16_t* out, int num_sms, cudaStream_t stream,
+                             bool pdl) {
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  PhaseParams& ph = prm.ph[0];
+  const int kdim = mode == 0 ? H : F;
+  const int planes = mode == 0 ? 2 : 1;
+  const int prows = mode == 0 ? F : H;
+  {
+    // gate/up: 64-row boxes (a CTA's 64 gate rows and the matching 64 up rows); down: 128 rows
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(prows),
+                                static_cast<cuuint64_t>(E) * planes};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kdim) * 2,
+                                   static_cast<cuuint64_t>(kdim) * 2 * static_cast<cuuint64_t>(prows)};
+    const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(mode == 0 ? 64 : kBM), 1};
+    if (!encode_map(&ph.tmap_w, weights, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim) * 2};
+    const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(kPairRows)};
+    if (!encode_map(&ph.tmap_x, act_in, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  ph.out = out;
+  ph.n_mb = mode == 0 ? F / kBM : H / (2 * kBM);
+  ph.ksteps = kdim / kBK;
+  ph.split = 1;
+  ph.out_ld = mode == 0 ? F : H;
+  ph.planes = planes;
+  prm.offsets = offsets;
+  prm.E = E;
+  prm.rows = rows;
+  return mode == 0 ? launch_pair_mode<0>(prm, num_sms, stream, pdl) : launch_pair_mode<1>(prm, num_sms, stream, pdl);
+}
+
 size_t gemm_scratch_bytes(const GemmPlan& gate_up, const GemmPlan& down) {
   return scratch_layout(gate_up, down).total;
 }
@@ -1382,6 +1759,7 @@ cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl) {
   const GemmPlan& plan = mode == 0 ? gate_up : down;
+  if (plan.pair) return launch_gemm_pair(mode, weights, act_in, offsets, rows, E, H, F, out, num_sms, stream, pdl);
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
   char* base = static_cast<char*>(scratch);

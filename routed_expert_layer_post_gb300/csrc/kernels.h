@@ -78,6 +78,7 @@ struct GemmPlan {
   int split;            // split-K factor (1 = no partial sums)
   int max_token_tiles;  // upper bound on (expert, token-tile) pairs
   int max_tiles;        // upper bound on (expert, row-block, token-tile) tiles
+  bool pair;            // prefill: paired-SM launch with 256-token tiles (launch_gemm_pair)
 };
 // mode 0: gate/up + SwiGLU (weight rows 2F, reduction H); mode 1: down (rows H, reduction F).
 // `fp4`: NVFP4 operands (256-value k-steps, token tiles of at most 32).
@@ -103,6 +104,11 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
                                  const uint16_t* w_down, const uint16_t* x_perm, const int32_t* offsets, int rows,
                                  int E, int H, int F, uint16_t* act, uint16_t* y_perm, void* scratch, int num_sms,
                                  cudaStream_t stream, bool pdl, const int* ready = nullptr);
+// One expert GEMM on CTA pairs (clusters of two, cta_group::2 MMAs, 256-token
+// tiles); mode 0 gate/up + SwiGLU, mode 1 down. Uses no scratch.
+cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* act_in, const int32_t* offsets,
+                             int rows, int E, int H, int F, uint16_t* out, int num_sms, cudaStream_t stream,
+                             bool pdl);
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl = false);

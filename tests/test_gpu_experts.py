@@ -46,6 +46,8 @@ def _sample_experts(counts, limit):
     ("decode_t1", 1024, 0.0, 12),     # token tile 64
     ("decode_t1", 2048, 1.1, 12),     # token tile 128, skewed loads
     ("decode_t1", 4096, 0.0, 8),      # down GEMM with 256-token tiles
+    ("toy", 1024, 1.5, None),         # paired-SM GEMMs: 256-token tiles, skewed, ragged tails
+    ("decode_t1", 8192, 1.1, 8),      # paired-SM GEMMs at Beam shapes
 ])
 def test_gate_up_and_down(name, T, skew, limit):
     beam = beam_module()
