@@ -932,9 +932,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 // through shared memory for SwiGLU. A pair covers 128 d_ff columns. Down: 128
 // rows of W_d per CTA, 256 per pair.
 //
-// Work: a static round-robin over tiles (expert, weight row block, 256-token
-// tile), both CTAs of a pair walking the same sequence (tiles are equal work,
-// and no tile waits on another). Roles (320 threads): warp 0 loads this CTA's
+// Work: tiles (expert, weight row block, 256-token tile) from the launch's
+// unit counter, taken by the leader and published to both CTAs' queues (no
+// tile waits on another). Roles (320 threads): warp 0 loads this CTA's
 // halves; warp 1 of the leader CTA (cluster rank 0) issues the MMAs of a stage
 // once both halves have landed and commits to both CTAs' barriers; warps 2-9
 // are two epilogue groups taking alternate tiles, each CTA reading its own
@@ -976,14 +976,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* xch = reinterpret_cast<float*>(tiles + kPairStages * kPairStageBytes);  // [group][16 columns][64 lanes]
   uint8_t* ctrl = tiles + kPairStages * kPairStageBytes + kPairXchBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);  // leader: both halves of a stage landed
   uint64_t* empty = full + kPairStages;
   uint64_t* tfull = empty + kPairStages;
-  uint64_t* tempty = tfull + 2;           // leader: both CTAs' epilogues released the accumulator
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + 2;    // leader: both CTAs' epilogues released the accumulator
+  uint64_t* qfull = tempty + 2;    // a unit id is in the queue slot (both CTAs)
+  uint64_t* qempty = qfull + kQueue;  // leader: the slot's four readers are done with it
+  uint64_t* drain = qempty + kQueue;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_off = s_flags + 8;
+  int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort; [4g+3] group g's current unit
+  int* s_queue = s_flags + 8;
+  int* s_off = s_queue + kQueue;
   int* s_ntt = s_off + kMaxE + 1;
   int* s_ttstart = s_ntt + kMaxE;
   volatile int* abort_flag = s_flags;
@@ -992,7 +995,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = ptx::cluster_rank();
   const bool leader = rank == 0;
-  const int pair = static_cast<int>(blockIdx.x) >> 1, npairs = static_cast<int>(gridDim.x) >> 1;
   if (tid == 0) {
     for (int i = 0; i < kPairStages; ++i) {
       ptx::mbar_init(&full[i], 1);
@@ -1001,6 +1003,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], 2);
+    }
+    for (int q = 0; q < kQueue; ++q) {
+      ptx::mbar_init(&qfull[q], 1);
+      ptx::mbar_init(&qempty[q], 4);  // leader: MMA thread and an epilogue group; peer: producer and a group
     }
     ptx::mbar_init(drain, 1);
     for (int i = 0; i < 8; ++i) s_flags[i] = 0;
@@ -1014,8 +1020,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc_pair(tmem_slot, kPairTmemCols);
     ptx::tmem_relinquish_pair();
   }
-  ptx::griddep_wait();  // offsets and activation rows come from the previous kernels
+  ptx::griddep_wait();  // offsets, activation rows and the zeroed unit counter come from earlier kernels
   ptx::griddep_launch_dependents();
+  int u_first = 0;
+  if (leader && tid == 0) u_first = atomicAdd(p.counter, 1);  // the round trip overlaps the set-up below
   for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
   __syncthreads();
   if (warp == 0) {
@@ -1051,18 +1059,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int n_units = s_ttstart[p.E] * ph.n_mb;
+  const uint32_t qempty0 = ptx::cluster_addr(qempty, 0);  // the leader's
+  const uint32_t qfull1 = ptx::cluster_addr(qfull, 1);    // the peer's
+  const uint32_t queue1 = ptx::cluster_addr(s_queue, 1);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (this CTA's halves)
+    // ------------------------------------------------------------ unit queue + TMA producer (this CTA's halves)
+    // The leader takes unit ids from the launch's counter in increasing
+    // order (tiles sharing weights run at the same time on neighbouring
+    // pairs, so the second reads them from L2) and publishes each id to both
+    // CTAs' queues; the peer's producer and both CTAs' MMA and epilogue
+    // roles read it from their own copy.
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
+      const uint32_t full0 = ptx::cluster_addr(full, 0);
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      // both CTAs' loads complete on the leader's full barrier, which expects the pair's bytes
-      const uint32_t full0 = ptx::cluster_addr(full, 0);
-      for (int u = pair; u < n_units && ok; u += npairs) {
+      int u_next = u_first;
+      for (int seq = 0;; ++seq) {
+        const int slot = seq % kQueue;
+        const uint32_t qpar = (seq / kQueue) & 1;
+        int u;
+        if (leader) {
+          u = (u_next < n_units && ok) ? u_next : -1;
+          const int nslots = u < 0 ? 2 : 1;  // the epilogue group of the next slot also needs the stop mark
+          for (int i = 0; i < nslots; ++i) {
+            const int sl = (seq + i) % kQueue;
+            if (!wait_bar_cluster(&qempty[sl], (((seq + i) / kQueue) & 1) ^ 1u, abort_flag, 39)) u = -1;
+            s_queue[sl] = u;
+            asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(queue1 + static_cast<uint32_t>(sl * 4)), "r"(u)
+                         : "memory");
+            ptx::mbar_arrive(&qfull[sl]);
+            ptx::mbar_arrive_remote(qfull1 + static_cast<uint32_t>(sl * sizeof(uint64_t)));
+          }
+          if (u < 0) break;
+          u_next = atomicAdd(p.counter, 1);  // the next id, while this unit's loads are issued
+        } else {
+          u = -1;
+          if (wait_bar_cluster(&qfull[slot], qpar, abort_flag, 40)) u = s_queue[slot];
+          ptx::mbar_arrive_remote(qempty0 + static_cast<uint32_t>(slot * sizeof(uint64_t)));
+          if (u < 0 || !ok) break;
+        }
         const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
         const int row0 = s_off[w.e] + w.tt * kPairN + static_cast<int>(rank) * kPairRows;
         for (int k = 0; k < ph.ksteps; ++k) {
@@ -1071,6 +1110,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* st = tiles + stage * kPairStageBytes;
+          // both CTAs' loads complete on the leader's full barrier, which expects the pair's bytes
           const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
           if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kPairStageBytes);
           if (MODE == 0) {
@@ -1099,46 +1139,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA only)
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      if (leader) {
-        constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kPairN);
-        int acc = 0;
-        uint32_t acc_phase = 0;
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kPairN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int seq = 0;; ++seq) {
+        const int slot = seq % kQueue;
+        int u = -1;
+        if (wait_bar(&qfull[slot], (seq / kQueue) & 1, abort_flag, 41, kTimeoutNs)) u = s_queue[slot];
+        ptx::mbar_arrive(&qempty[slot]);
+        if (u < 0) break;
+        if (!wait_bar_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, 33)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
         bool ok = true;
-        for (int u = pair; u < n_units && ok; u += npairs) {
-          if (!wait_bar_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, 33)) break;
-          ptx::tc_fence_after();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
-          for (int k = 0; k < ph.ksteps; ++k) {
-            if (!wait_bar_cluster(&full[stage], phase, abort_flag, 34)) {  // both halves landed
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t sa = ptx::smem_u32(tiles + stage * kPairStageBytes);
-            const uint32_t sb = sa + kTileABytes;
-#pragma unroll
-            for (int j = 0; j < kBK / 16; ++j)
-              ptx::mma_bf16_pair(d, ptx::smem_desc_k128(sa + j * 32), ptx::smem_desc_k128(sb + j * 32), idesc,
-                                 (k > 0 || j > 0) ? 1u : 0u);
-            ptx::mma_commit_pair(&empty[stage]);
-            if (++stage == kPairStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
+        for (int k = 0; k < ph.ksteps; ++k) {
+          if (!wait_bar_cluster(&full[stage], phase, abort_flag, 34)) {  // both halves landed
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          ptx::mma_commit_pair(&tfull[acc]);
-          if (++acc == 2) {
-            acc = 0;
-            acc_phase ^= 1u;
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(tiles + stage * kPairStageBytes);
+          const uint32_t sb = sa + kTileABytes;
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j)
+            ptx::mma_bf16_pair(d, ptx::smem_desc_k128(sa + j * 32), ptx::smem_desc_k128(sb + j * 32), idesc,
+                               (k > 0 || j > 0) ? 1u : 0u);
+          ptx::mma_commit_pair(&empty[stage]);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        ptx::mma_commit_pair(drain);  // every MMA of the pair issued here has completed once `drain` flips
-        wait_bar(drain, 0, nullptr, 36, kTimeoutNs);
+        if (!ok) break;
+        ptx::mma_commit_pair(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
+      ptx::mma_commit_pair(drain);  // every MMA of the pair issued here has completed once `drain` flips
+      wait_bar(drain, 0, nullptr, 36, kTimeoutNs);
     }
   } else {
     // ------------------------------------------------------------ epilogue groups (warps 2-5, 6-9)
@@ -1147,13 +1188,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int m = sub * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
     const uint32_t bar_id = 1 + eg;
+    const bool group_leader = (warp == 2 + 4 * eg && lane == 0);
+    int* g_unit = s_flags + 4 * eg + 3;
     float* x = xch + eg * 64 * 16;
     const uint32_t tempty_leader = ptx::cluster_addr(&tempty[eg], 0);
     uint32_t acc_phase = 0;
-    for (int i = eg;; i += 2) {
-      const int u = pair + i * npairs;
-      if (u >= n_units) break;
-      if (!wait_bar(&tfull[eg], acc_phase, abort_flag, 38, kTimeoutNs)) break;
+    for (int seq = eg;; seq += 2) {
+      if (group_leader) {
+        const int slot = seq % kQueue;
+        int u = -1;
+        if (wait_bar_cluster(&qfull[slot], (seq / kQueue) & 1, abort_flag, 42)) u = s_queue[slot];
+        if (leader) ptx::mbar_arrive(&qempty[slot]);
+        else ptx::mbar_arrive_remote(qempty0 + static_cast<uint32_t>(slot * sizeof(uint64_t)));
+        if (u >= 0 && !wait_bar(&tfull[eg], acc_phase, abort_flag, 38, kTimeoutNs)) u = -1;
+        *g_unit = u;
+      }
+      ptx::named_bar_sync(bar_id, 128);
+      const int u = *reinterpret_cast<volatile int*>(g_unit);
+      ptx::named_bar_sync(bar_id, 128);
+      if (u < 0) break;
       ptx::tc_fence_after();
       const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
       const int row0 = s_off[w.e] + w.tt * kPairN;
@@ -1192,7 +1245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::named_bar_sync(bar_id, 128);
-      if (warp == 2 + 4 * eg && lane == 0) {
+      if (group_leader) {
         if (leader) ptx::mbar_arrive(&tempty[eg]);
         else ptx::mbar_arrive_remote(tempty_leader);
       }
@@ -1708,8 +1761,8 @@ cudaError_t launch_pair_mode(const GemmParams& prm, int num_sms, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* act_in, const int32_t* offsets,
-                             int rows, int E, int H, int F, uint16_t* out, int num_sms, cudaStream_t stream,
-                             bool pdl) {
+                             int rows, int E, int H, int F, uint16_t* out, int* counter, int num_sms,
+                             cudaStream_t stream, bool pdl) {
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
   PhaseParams& ph = prm.ph[0];
@@ -1738,6 +1791,7 @@ cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* 
   ph.out_ld = mode == 0 ? F : H;
   ph.planes = planes;
   prm.offsets = offsets;
+  prm.counter = counter;
   prm.E = E;
   prm.rows = rows;
   return mode == 0 ? launch_pair_mode<0>(prm, num_sms, stream, pdl) : launch_pair_mode<1>(prm, num_sms, stream, pdl);
@@ -1759,7 +1813,9 @@ cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl) {
   const GemmPlan& plan = mode == 0 ? gate_up : down;
-  if (plan.pair) return launch_gemm_pair(mode, weights, act_in, offsets, rows, E, H, F, out, num_sms, stream, pdl);
+  if (plan.pair)
+    return launch_gemm_pair(mode, weights, act_in, offsets, rows, E, H, F, out, static_cast<int*>(scratch) + mode,
+                            num_sms, stream, pdl);
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
   char* base = static_cast<char*>(scratch);

@@ -105,10 +105,11 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
                                  int E, int H, int F, uint16_t* act, uint16_t* y_perm, void* scratch, int num_sms,
                                  cudaStream_t stream, bool pdl, const int* ready = nullptr);
 // One expert GEMM on CTA pairs (clusters of two, cta_group::2 MMAs, 256-token
-// tiles); mode 0 gate/up + SwiGLU, mode 1 down. Uses no scratch.
+// tiles); mode 0 gate/up + SwiGLU, mode 1 down. `counter`: the launch's unit
+// counter, zero before the launch.
 cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* act_in, const int32_t* offsets,
-                             int rows, int E, int H, int F, uint16_t* out, int num_sms, cudaStream_t stream,
-                             bool pdl);
+                             int rows, int E, int H, int F, uint16_t* out, int* counter, int num_sms,
+                             cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm(int mode, const GemmPlan& gate_up, const GemmPlan& down, const uint16_t* weights,
                         const uint16_t* act_in, const int32_t* offsets, int rows, int E, int H, int F, uint16_t* out,
                         void* scratch, int num_sms, cudaStream_t stream, bool pdl = false);
