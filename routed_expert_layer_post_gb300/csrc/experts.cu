@@ -68,6 +68,7 @@ struct PhaseParams {
   CUtensorMap tmap_w;   // weights, 3-D: (k, row, plane); expert e owns planes e*planes .. +planes-1
   CUtensorMap tmap_x;   // activations, 2-D: (k, permuted row)
   CUtensorMap tmap_sfx; // NVFP4: activation scale slots, 2-D: (16-byte slot, permuted row)
+  CUtensorMap tmap_x16; // paired-SM GEMMs: activations with a 16-row box (narrow last token tiles)
   uint16_t* out;        // bf16 output (down; gate/up of the bf16 path)
   uint8_t* out_q;       // NVFP4 gate/up: codes of the SwiGLU output [rows][F/2]
   uint8_t* out_sf;      // NVFP4 gate/up: its scale slots [rows][F/64][16]
@@ -359,23 +360,35 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   // however many of its CTAs are resident (another kernel may hold SMs).
   // Thread 0 (the producer) requests its first id as soon as the counter is
   // known to be zeroed; the round trip overlaps the tile-table set-up.
-  int u_first = 0;
+  // The producer holds the ids of its next two units: under full HBM load an
+  // atomic's round trip takes several microseconds (it queues behind the
+  // streaming loads), longer than an NVFP4 unit's loads, so the id of unit
+  // n + 2 is requested when unit n starts.
+  int u_first = 0, u_second = 0;
   if (MODE != 1) {
     if (MODE == 2 && p.ready != nullptr) {
       if (tid == 0) {
-        if (!wait_counter(p.ready, 1, abort_flag, 9)) s_flags[2] = 1;
-        else u_first = atomicAdd(p.counter, 1);
+        if (!wait_counter(p.ready, 1, abort_flag, 9)) {
+          s_flags[2] = 1;
+        } else {
+          u_first = atomicAdd(p.counter, 1);
+          u_second = atomicAdd(p.counter, 1);
+        }
       }
       __syncthreads();  // thread 0's acquire orders the offset and counter reads below
     } else {
       ptx::griddep_wait();
-      if (tid == 0) u_first = atomicAdd(p.counter, 1);
+      if (tid == 0) {
+        u_first = atomicAdd(p.counter, 1);
+        u_second = atomicAdd(p.counter, 1);
+      }
     }
     ptx::griddep_launch_dependents();
   } else if (tid == 0) {
     // the down GEMM's counter was zeroed two kernels back (the permutation),
     // which completed before the gate/up GEMM let this launch start
     u_first = atomicAdd(p.counter, 1);
+    u_second = atomicAdd(p.counter, 1);
   }
   for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
   __syncthreads();
@@ -446,9 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler + TMA producer
-    // Units are handed out dynamically from a global counter (the next id
-    // is requested while the current unit's loads are issued), so SMs that
-    // stream faster take more units and all SMs finish together. Each unit
+    // Units are handed out dynamically from a global counter (the id of the
+    // unit after next is requested while the current unit's loads are
+    // issued), so SMs that stream faster take more units and all SMs finish
+    // together. Each unit
     // id is published to the MMA and epilogue warps through a small queue in
     // shared memory.
     if (lane == 0) {
@@ -507,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         ready_gtt = pend_gtt;
         return true;
       };
-      int u_next = u_first;
+      int u_next = u_first, u_after = u_second;
       for (int seq = 0;; ++seq) {
         int u = u_next;
         if (u >= n_units || !ok) u = -1;
@@ -534,8 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           ptx::mbar_arrive(&qfull[s2]);
           break;
         }
-        // ask for the following unit now: the atomic's round trip overlaps this unit's loads
-        u_next = atomicAdd(p.counter, 1);
+        // ask for the unit after the next one now: the round trip overlaps two units' loads
+        u_next = u_after;
+        u_after = atomicAdd(p.counter, 1);
         const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
@@ -932,6 +947,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
 // through shared memory for SwiGLU. A pair covers 128 d_ff columns. Down: 128
 // rows of W_d per CTA, 256 per pair.
 //
+// Narrow last tiles: an expert's rows rarely fill its last 256-token tile
+// (at 16384 tokens and 256 experts, 256-wide tiles would compute 19 % empty
+// columns). That tile runs as an MMA of width N = its rows rounded up to 32;
+// each CTA then supplies N/2 token rows (CTA 0 the first half, CTA 1 the
+// second, so accumulator column c is still the tile's token c), loaded as
+// 16-row boxes.
+//
 // Work: tiles (expert, weight row block, 256-token tile) from the launch's
 // unit counter, taken by the leader and published to both CTAs' queues (no
 // tile waits on another). Roles (320 threads): warp 0 loads this CTA's
@@ -946,6 +968,12 @@ constexpr int kPairXchBytes = 2 * 64 * 16 * 4;                     // SwiGLU exc
 constexpr int kPairStages = (kSmemLimit - 1024 - kCtrlBytes - kPairXchBytes) / kPairStageBytes;
 constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + kPairXchBytes + kCtrlBytes;
 constexpr int kPairTmemCols = 2 * kPairN;                          // two accumulator buffers
+
+// MMA width (tokens) of a tile holding `valid` rows: the full 256, or for an
+// expert's last, partly filled tile the rows rounded up to 32, so that the
+// tensor cores skip the empty columns (each CTA then loads and supplies half
+// of the width, 16 rows per TMA box).
+__device__ __forceinline__ int pair_width(int valid) { return valid >= kPairN ? kPairN : (valid + 31) & ~31; }
 static_assert(kPairStages >= 6, "six 32 KB stages per SM");
 
 // Bounded wait at cluster scope (for barriers the other CTA arrives on).
@@ -1015,6 +1043,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&ph.tmap_w);
     ptx::prefetch_tensormap(&ph.tmap_x);
+    ptx::prefetch_tensormap(&ph.tmap_x16);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(tmem_slot, kPairTmemCols);
@@ -1071,7 +1100,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // CTAs' queues; the peer's producer and both CTAs' MMA and epilogue
     // roles read it from their own copy.
     if (lane == 0) {
-      const uint64_t pol_w = ptx::policy_evict_first();
+      // a weight tile is read by the pairs running the expert's two or three
+      // token tiles at about the same time: normal priority keeps it in L2
+      // between them (evict-first measured 2 % slower at 16384 tokens)
+      const uint64_t pol_w = ptx::policy_evict_normal();
       const uint64_t pol_x = ptx::policy_evict_last();
       const uint32_t full0 = ptx::cluster_addr(full, 0);
       int stage = 0, issued = 0;
@@ -1103,7 +1135,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (u < 0 || !ok) break;
         }
         const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
-        const int row0 = s_off[w.e] + w.tt * kPairN + static_cast<int>(rank) * kPairRows;
+        const int base_row = s_off[w.e] + w.tt * kPairN;
+        const int half = pair_width(s_off[w.e + 1] - base_row) / 2;  // token rows this CTA supplies
+        const int row0 = base_row + static_cast<int>(rank) * half;
+        const uint32_t stage_tx = 2u * static_cast<uint32_t>(kTileABytes + half * kBK * 2);
         for (int k = 0; k < ph.ksteps; ++k) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, 31, kTimeoutNs)) {
             ok = false;
@@ -1112,7 +1147,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* st = tiles + stage * kPairStageBytes;
           // both CTAs' loads complete on the leader's full barrier, which expects the pair's bytes
           const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
-          if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kPairStageBytes);
+          if (leader) ptx::mbar_arrive_expect_tx(&full[stage], stage_tx);
           if (MODE == 0) {
             const int f0 = w.mb * kBM + static_cast<int>(rank) * 64;
             ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, f0, 2 * w.e, pol_w);                    // gate rows
@@ -1121,7 +1156,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, w.mb * 2 * kBM + static_cast<int>(rank) * kBM, w.e,
                                   pol_w);
           }
-          ptx::tma_load_2d_pair(st + kTileABytes, &ph.tmap_x, fb, k * kBK, row0, pol_x);
+          if (half == kPairRows) {
+            ptx::tma_load_2d_pair(st + kTileABytes, &ph.tmap_x, fb, k * kBK, row0, pol_x);
+          } else {
+            for (int i = 0; i < half; i += 16)
+              ptx::tma_load_2d_pair(st + kTileABytes + i * kBK * 2, &ph.tmap_x16, fb, k * kBK, row0 + i, pol_x);
+          }
           ++issued;
           if (++stage == kPairStages) {
             stage = 0;
@@ -1140,7 +1180,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA only)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kPairN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int seq = 0;; ++seq) {
@@ -1149,6 +1188,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (wait_bar(&qfull[slot], (seq / kQueue) & 1, abort_flag, 41, kTimeoutNs)) u = s_queue[slot];
         ptx::mbar_arrive(&qempty[slot]);
         if (u < 0) break;
+        const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
+        const int base_row = s_off[w.e] + w.tt * kPairN;
+        const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, pair_width(s_off[w.e + 1] - base_row));
         if (!wait_bar_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, 33)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
@@ -1783,6 +1825,8 @@ cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* 
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim) * 2};
     const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(kPairRows)};
     if (!encode_map(&ph.tmap_x, act_in, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const cuuint32_t box16[2] = {kBK, 16};
+    if (!encode_map(&ph.tmap_x16, act_in, 2, dims, strides, box16)) return cudaErrorInvalidValue;
   }
   ph.out = out;
   ph.n_mb = mode == 0 ? F / kBM : H / (2 * kBM);

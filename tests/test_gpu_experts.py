@@ -50,11 +50,45 @@ def _sample_experts(counts, limit):
     ("decode_t1", 8192, 1.1, 8),      # paired-SM GEMMs at Beam shapes
 ])
 def test_gate_up_and_down(name, T, skew, limit):
-    beam = beam_module()
     m = model(name)
+    ids, z_bits, counts, offsets, perm, inv, xp_bits = _inputs(m, T, skew, seed=T * 7 + 1)
+    _check_gate_up_and_down(m, T, counts, offsets, xp_bits, limit)
+
+
+def _ids_with_counts(counts, T, K):
+    """Routing ids [T][K] in which expert e is chosen by counts[e] tokens,
+    each token's K experts distinct: the experts' slots laid out expert by
+    expert and dealt column by column (a block of at most T consecutive
+    slots never meets the same token twice)."""
+    assert sum(counts) == T * K and max(counts) <= T
+    slots = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    return slots.reshape(K, T).T.copy()
+
+
+def test_paired_gemm_tail_widths():
+    """Paired-SM GEMMs (256-token tiles) with every kind of last tile: the
+    experts' row counts leave 1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128,
+    129 and 200 rows in the last tile, one expert fills its last tile exactly
+    and the last one takes the remaining rows (1127: a fifth tile of 103)."""
+    m = model("toy")
+    cfg = m.cfg
+    tails = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200, 256]
+    counts = [256 + t for t in tails]
+    T = 1536
+    counts.append(T * cfg.K - sum(counts))
+    assert counts[-1] == 1127
+    ids = _ids_with_counts(counts, T, cfg.K)
+    rng = np.random.default_rng(17)
+    z_bits = obf.encode(rng.standard_normal((T, cfg.H)))
+    cnt, offsets, perm, inv = permute(ids, cfg.E)
+    assert list(cnt) == counts
+    _check_gate_up_and_down(m, T, cnt, offsets, z_bits[perm], None)
+
+
+def _check_gate_up_and_down(m, T, counts, offsets, xp_bits, limit):
+    beam = beam_module()
     cfg = m.cfg
     mc = beam.make_config(cfg.H, cfg.E, cfg.G, cfg.TG, cfg.K, cfg.F, cfg.routed_scale, cfg.eps)
-    ids, z_bits, counts, offsets, perm, inv, xp_bits = _inputs(m, T, skew, seed=T * 7 + 1)
     off_d = torch.from_numpy(offsets).cuda()
     act = beam.beam_moe_gate_up(dev_bf16(xp_bits), off_d, m.dev[0], mc, T)
     # the down GEMM takes the oracle's rounded intermediate, so the two GEMMs are checked independently
