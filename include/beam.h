@@ -319,7 +319,10 @@ beam_status_t beam_moe_experts_nvfp4(const uint16_t* x_perm, const int32_t* expe
 
 /* beam_moe_layer with NVFP4 experts: the same boundary, FP32 routing and
  * permutation, then beam_moe_experts_nvfp4. dbg as for beam_moe_layer (its
- * stage event [3] is recorded after the input quantization). */
+ * stage event [3] is recorded after the input quantization). At decode sizes
+ * (T <= 8, 256 experts in 8 groups) the routing launch writes the permuted
+ * rows already quantized (the same codes and scales as
+ * beam_nvfp4_quantize_rows), and the expert launch starts on its flags. */
 size_t beam_moe_nvfp4_workspace_size(const beam_moe_config_t* cfg, int T);
 beam_status_t beam_moe_layer_nvfp4(const uint16_t* h, const uint16_t* x, int n,
                                    const beam_moe_nvfp4_weights_t* weights, int T,

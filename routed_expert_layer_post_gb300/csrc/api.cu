@@ -206,12 +206,14 @@ beam_status_t run_experts(const uint16_t* x_perm, const int32_t* offsets, const 
 // both GEMMs in one launch (the SwiGLU output quantized with g_act), then
 // the combine. `cleared`: the GEMM counters and tickets were zeroed by an
 // earlier kernel. `inter` (optional) receives the workspace addresses of the
-// intermediates.
+// intermediates. `ready` (decode routing): the routing kernel already wrote
+// the quantized rows to the workspace and raises these flags; the experts
+// launch polls them (x_perm is not read).
 beam_status_t run_experts_fp4(const uint16_t* x_perm, const int32_t* offsets, const beam::Nvfp4Experts& wt,
                               float g_in, float g_act, const float* topk_w, const int32_t* inv, int T,
                               const beam_moe_config_t* c, uint16_t* y, char* ws, int sms, cudaStream_t s,
                               const beam_moe_debug_t* dbg, bool pdl, bool cleared, int* err_out,
-                              beam_moe_nvfp4_intermediates_t* inter) {
+                              beam_moe_nvfp4_intermediates_t* inter, const int* ready = nullptr) {
   const ExpertsWsFp4 w = experts_ws_fp4(c, T, sms);
   const int rows = T * c->topk;
   uint8_t* xq = reinterpret_cast<uint8_t*>(ws + w.xq);
@@ -225,11 +227,11 @@ beam_status_t run_experts_fp4(const uint16_t* x_perm, const int32_t* offsets, co
   beam::plan_experts(T, c->topk, c->num_experts, c->hidden, c->d_ff, sms, &p0, &p1, /*fp4=*/true);
   cudaError_t e = cudaSuccess;
   if (!cleared && (e = beam::clear_gemm_scratch(g, p0, p1, s)) != cudaSuccess) return BEAM_ERR_CUDA;
-  if ((e = beam::launch_quantize_rows(x_perm, rows, c->hidden, g_in, xq, xsf, s, pdl)) != cudaSuccess)
+  if (ready == nullptr && (e = beam::launch_quantize_rows(x_perm, rows, c->hidden, g_in, xq, xsf, s, pdl)) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(dbg, 3, s);
   e = beam::launch_fused_experts_fp4(p0, p1, wt, xq, xsf, g_in, offsets, rows, c->num_experts, c->hidden, c->d_ff,
-                                     aq, asf, g_act, y_perm, g, sms, s, pdl);
+                                     aq, asf, g_act, y_perm, g, sms, s, pdl, ready);
   if (e != cudaSuccess) return BEAM_ERR_CUDA;
   record(dbg, 4, s);
   record(dbg, 5, s);
@@ -504,10 +506,16 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
     // decode sizes: boundary, router, top-k, permutation and the GEMM scratch
     // clear in one launch (the stage events of router and permutation are
     // empty); the fused experts launch starts on the routing kernel's flags
+    // NVFP4 experts: the routing kernel writes the permuted rows quantized
+    const ExpertsWsFp4 wq = fp4 ? experts_ws_fp4(cfg, T, d.sms) : ExpertsWsFp4{};
+    const bool fp4_rows = fp4 && beam::fused_experts_supported(p0, p1);
+    uint8_t* xq = fp4_rows ? reinterpret_cast<uint8_t*>(base + L.experts + wq.xq) : nullptr;
+    uint8_t* xsf = fp4_rows ? reinterpret_cast<uint8_t*>(base + L.experts + wq.xsf) : nullptr;
     e = beam::launch_route_decode(h, x, wt->w_post, wt->w_pre, wt->router_w, wt->bias, T, H, cfg->num_experts,
                                   cfg->num_groups, cfg->topk_groups, cfg->topk, cfg->routed_scale, cfg->eps, n,
                                   h_out, z, logits, ids, w, offsets, perm, inv, x_perm, router_ticket, gemm_scratch,
-                                  beam::gemm_clear_bytes(p0, p1), d.sms, s, pdl, route_sync_zeroed);
+                                  beam::gemm_clear_bytes(p0, p1), d.sms, s, pdl, route_sync_zeroed, xq, xsf,
+                                  fp4 ? fp4w->input_scale : 0.f);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
     record(dbg, 1, s);
     record(dbg, 2, s);
@@ -515,7 +523,8 @@ static beam_status_t layer_impl(const uint16_t* h, const uint16_t* x, int n, con
     launch_counter() = 0;
     if (fp4) {
       st = run_experts_fp4(x_perm, offsets, nvfp4_of(fp4w), fp4w->input_scale, fp4w->act_scale, w, inv, T, cfg,
-                           y_out, base + L.experts, d.sms, s, dbg, pdl, /*cleared=*/true, err_out, nullptr);
+                           y_out, base + L.experts, d.sms, s, dbg, pdl, /*cleared=*/true, err_out, nullptr,
+                           fp4_rows ? router_ticket + 1 : nullptr);
     } else {
       const int* ready = beam::fused_experts_supported(p0, p1) ? router_ticket + 1 : nullptr;
       st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, y_out, base + L.experts, d.sms,

@@ -50,6 +50,14 @@ namespace {
 // two epilogue groups taking alternate units (each group covers the four
 // TMEM lane quarters), so one group's split-K round trips overlap the other's
 constexpr int kThreads = 320;
+// The single-CTA GEMM adds a watcher warp (warp 10): in the fused launch it
+// polls the token tiles' gate/up completion counters and mirrors them in
+// shared memory, so the producer never waits on a global round trip (under
+// full HBM load one takes several microseconds) to learn that a down unit's
+// rows are complete.
+constexpr int kWatchWarp = kThreads / 32;
+constexpr int kGemmThreads = kThreads + 32;
+constexpr int kMaxWatchTiles = 2048;  // token tiles the shared-memory mirror holds (one bit each)
 constexpr int kEpiGroups = 2;
 constexpr int kBM = 128;                     // weight rows per tile (MMA M)
 constexpr int kBK = 64;                      // reduction elements per stage: 128 bytes of bf16
@@ -183,6 +191,20 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
+// Shared-memory bits with release/acquire semantics at CTA scope: the watcher
+// warp sets a token tile's bit after its GPU-scope acquire of the tile's
+// completion counter; the producer's acquire of the bit then orders the rows
+// the counter published before its own loads.
+__device__ __forceinline__ void smem_or_release(uint32_t* w, uint32_t bits) {
+  asm volatile("red.release.cta.shared::cta.or.b32 [%0], %1;" ::"r"(ptx::smem_u32(w)), "r"(bits) : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_ld_acquire(const uint32_t* w) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(ptx::smem_u32(w)) : "memory");
+  return v;
+}
+
 // Wait (bounded) until *counter >= target; other CTAs of this launch raise it.
 __device__ __forceinline__ bool wait_counter(const int* counter, int target, volatile int* abort_flag, int site,
                                              uint64_t limit_ns = kTimeoutNs) {
@@ -208,6 +230,17 @@ struct Unit {
   int phase, e, mb, tt, gtt, s, tile;
 };
 
+// Expert owning global token tile j: the largest e with s_ttstart[e] <= j
+// (experts without rows start where the next one does).
+__device__ __forceinline__ int tile_owner(int j, int E, const int* s_ttstart) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_ttstart[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // Tiles of a phase are laid out expert by expert, row block by row block,
 // token tile fastest; expert e's tiles start at n_mb * s_ttstart[e].
 // `rot0` (fused launch): phase-0 tiles are taken starting at tile rot0 (an
@@ -225,12 +258,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int n_units0, const GemmParam
     if (r.tile >= n_tiles0) r.tile -= n_tiles0;
   }
   const int q = r.tile / ph.n_mb;
-  int lo = 0, hi = p.E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_ttstart[mid] <= q) lo = mid; else hi = mid - 1;
-  }
-  r.e = lo;
+  r.e = tile_owner(q, p.E, s_ttstart);
   const int local = r.tile - ph.n_mb * s_ttstart[r.e];
   const int ntt = s_ntt[r.e];
   r.mb = local / ntt;
@@ -291,7 +319,7 @@ __device__ __forceinline__ size_t sf_atoms(const PhaseParams& ph, int plane, int
 }
 
 template <int MODE, int BN, bool FP4>
-__global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<MODE, BN, FP4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles =
@@ -305,12 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   uint64_t* qempty = qfull + kQueue;
   uint64_t* drain = qempty + kQueue;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  // [0] abort; per epilogue group g: [4g+1] last arriver, [4g+3] current unit
+  // [0] abort; [2] routing flags never came; [4] the producer has finished;
+  // [6] the routing rows flag was seen; per epilogue group g: [4g+1] last
+  // arriver, [4g+3] current unit
   int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);
   int* s_queue = s_flags + 8;
   int* s_off = s_queue + kQueue;
   int* s_ntt = s_off + kMaxE + 1;
   int* s_ttstart = s_ntt + kMaxE;
+  uint32_t* s_tile_done = reinterpret_cast<uint32_t*>(s_ttstart + kMaxE + 1);  // MODE 2: watcher bits
+  uint32_t* s_rows = reinterpret_cast<uint32_t*>(s_flags + 6);  // MODE 2: the routing rows flag was seen
   volatile int* abort_flag = s_flags;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -360,37 +392,27 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   // however many of its CTAs are resident (another kernel may hold SMs).
   // Thread 0 (the producer) requests its first id as soon as the counter is
   // known to be zeroed; the round trip overlaps the tile-table set-up.
-  // The producer holds the ids of its next two units: under full HBM load an
-  // atomic's round trip takes several microseconds (it queues behind the
-  // streaming loads), longer than an NVFP4 unit's loads, so the id of unit
-  // n + 2 is requested when unit n starts.
-  int u_first = 0, u_second = 0;
+  int u_first = 0;
   if (MODE != 1) {
     if (MODE == 2 && p.ready != nullptr) {
       if (tid == 0) {
-        if (!wait_counter(p.ready, 1, abort_flag, 9)) {
-          s_flags[2] = 1;
-        } else {
-          u_first = atomicAdd(p.counter, 1);
-          u_second = atomicAdd(p.counter, 1);
-        }
+        if (!wait_counter(p.ready, 1, abort_flag, 9)) s_flags[2] = 1;
+        else u_first = atomicAdd(p.counter, 1);
       }
       __syncthreads();  // thread 0's acquire orders the offset and counter reads below
     } else {
       ptx::griddep_wait();
-      if (tid == 0) {
-        u_first = atomicAdd(p.counter, 1);
-        u_second = atomicAdd(p.counter, 1);
-      }
+      if (tid == 0) u_first = atomicAdd(p.counter, 1);
     }
     ptx::griddep_launch_dependents();
   } else if (tid == 0) {
     // the down GEMM's counter was zeroed two kernels back (the permutation),
     // which completed before the gate/up GEMM let this launch start
     u_first = atomicAdd(p.counter, 1);
-    u_second = atomicAdd(p.counter, 1);
   }
-  for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.offsets[i];
+  for (int i = tid; i <= p.E; i += kGemmThreads) s_off[i] = p.offsets[i];
+  if (MODE == 2)
+    for (int i = tid; i < kMaxWatchTiles / 32; i += kGemmThreads) s_tile_done[i] = 0u;
   __syncthreads();
   if (warp == 0) {
     // token tiles per expert and their exclusive prefix (lane l owns a contiguous block of experts)
@@ -433,36 +455,34 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
   }
   if (MODE == 2 && s_flags[2]) n_tiles0 = 0;  // the routing flags never came: do nothing
   const int n_units0 = n_tiles0 * p.ph[0].split;
+  const bool watch = MODE == 2 && n_tt <= kMaxWatchTiles;  // the watcher warp mirrors the tiles' completion
   // Fused launch: the first wave of gate/up units goes to the last experts.
   // Their epilogues run first on every SM, with cold instructions under full
   // HBM load, and finish late; the down units of those experts come last, so
   // nothing waits on them. rot0 is the start of the earliest expert such that
-  // the experts from it to the end hold at least one wave of units.
+  // the experts from it to the end hold at least one wave of units. (Handing
+  // each token tile's down units out a few tiles after its gate/up units,
+  // interleaved with the later gate/up units, measured slower: 1.28 against
+  // 1.01 ms at 64 tokens with NVFP4 experts, 128 against 122 us at one token
+  // in bf16.)
   int rot0 = 0;
   if (MODE == 2 && n_tiles0 > 0) {
     const int wave_tiles = (static_cast<int>(gridDim.x) + p.ph[0].split - 1) / p.ph[0].split;
     const int limit = n_tiles0 - wave_tiles;
-    if (limit > 0) {
-      int lo = 0, hi = p.E - 1;  // largest e with n_mb * s_ttstart[e] <= limit
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.ph[0].n_mb * s_ttstart[mid] <= limit) lo = mid; else hi = mid - 1;
-      }
-      rot0 = p.ph[0].n_mb * s_ttstart[lo];
-    }
+    if (limit > 0) rot0 = p.ph[0].n_mb * s_ttstart[tile_owner(limit / p.ph[0].n_mb, p.E, s_ttstart)];
   }
   int n_units = n_units0;
   if (MODE == 2 && n_tiles0 > 0) {
     const int n_tiles1 = n_tt * p.ph[1].n_mb;
     if (n_tiles1 <= p.ph[1].max_tiles) n_units += n_tiles1 * p.ph[1].split;
   }
+  auto decode = [&](int u) -> Unit { return decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler + TMA producer
-    // Units are handed out dynamically from a global counter (the id of the
-    // unit after next is requested while the current unit's loads are
-    // issued), so SMs that stream faster take more units and all SMs finish
-    // together. Each unit
+    // Units are handed out dynamically from a global counter (the next id
+    // is requested while the current unit's loads are issued), so SMs that
+    // stream faster take more units and all SMs finish together. Each unit
     // id is published to the MMA and epilogue warps through a small queue in
     // shared memory.
     if (lane == 0) {
@@ -494,12 +514,29 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
                                (4 * (k + h) + c) * 16, row, pol_x);
         }
       };
+      // MODE 2: the routing kernel's second flag (permuted rows valid), as
+      // mirrored in shared memory by the watcher warp
+      auto rows_seen = [&]() -> bool { return smem_ld_acquire(s_rows) != 0u; };
       auto release_pending = [&]() {
         if (MODE == 1) {
           ptx::griddep_wait();
           ptx::griddep_launch_dependents();
         } else {
-          if (!wait_counter(p.ready + 1, 1, abort_flag, 10)) ok = false;
+          if (!rows_seen()) {
+            const uint64_t t0 = ptx::globaltimer();
+            for (uint32_t it = 1;; ++it) {
+              __nanosleep(32);
+              if (rows_seen()) break;
+              if ((it & 15u) == 0 && (*abort_flag || ptx::globaltimer() - t0 > kTimeoutNs)) {
+                if (!*abort_flag) {
+                  *abort_flag = 1;
+                  atomicCAS(&g_device_error, 0, 10);
+                }
+                ok = false;
+                break;
+              }
+            }
+          }
           asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
         }
         for (int i = 0; i < npend; ++i) load_b(p.ph[0], pend_stage[i], pend_k[i], pend_row[i], false);
@@ -513,15 +550,39 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       // that tile are done, the ring is full, or the unit queue would block
       int pend_gtt = -1, pend_seq0 = 0;
       bool pend_two[C::kStages];
+      // MODE 2: has token tile j's gate/up output been seen complete? From
+      // the watcher warp's shared-memory bits (no global round trip), or, for
+      // more tiles than the bits hold, from the counter itself.
+      auto tile_done = [&](int j) -> bool {
+        if (watch) return (smem_ld_acquire(&s_tile_done[j >> 5]) >> (j & 31)) & 1u;
+        return ld_acquire(p.done + j) >= p.ph[0].n_mb;
+      };
+      auto wait_tile = [&](int j) -> bool {
+        if (!watch) return wait_counter(p.done + j, p.ph[0].n_mb, abort_flag, 8);
+        if (tile_done(j)) return true;
+        const uint64_t t0 = ptx::globaltimer();
+        for (uint32_t it = 1;; ++it) {
+          __nanosleep(32);
+          if (tile_done(j)) return true;
+          if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - t0 > kTimeoutNs) {
+              *abort_flag = 1;
+              atomicCAS(&g_device_error, 0, 8);
+              return false;
+            }
+          }
+        }
+      };
       auto release_down = [&]() -> bool {
-        if (!wait_counter(p.done + pend_gtt, p.ph[0].n_mb, abort_flag, 8)) return false;
+        if (!wait_tile(pend_gtt)) return false;
         asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what generic stores wrote
         for (int i = 0; i < npend; ++i) load_b(p.ph[1], pend_stage[i], pend_k[i], pend_row[i], pend_two[i]);
         npend = 0;
         ready_gtt = pend_gtt;
         return true;
       };
-      int u_next = u_first, u_after = u_second;
+      int u_next = u_first;
       for (int seq = 0;; ++seq) {
         int u = u_next;
         if (u >= n_units || !ok) u = -1;
@@ -548,10 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           ptx::mbar_arrive(&qfull[s2]);
           break;
         }
-        // ask for the unit after the next one now: the round trip overlaps two units' loads
-        u_next = u_after;
-        u_after = atomicAdd(p.counter, 1);
-        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
+        // ask for the following unit now: the atomic's round trip overlaps this unit's loads
+        u_next = atomicAdd(p.counter, 1);
+        const Unit w = decode(u);
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
         const int nacc = kind == 0 ? 2 : 1;
@@ -565,14 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           // running CTAs (all gate/up units are handed out before any down
           // unit). Deferred stages are always the newest in the ring: a unit
           // of another token tile first releases them.
-          if (npend > 0 && (pend_gtt != w.gtt || ld_acquire(p.done + pend_gtt) >= p.ph[0].n_mb)) {
+          if (npend > 0 && (pend_gtt != w.gtt || tile_done(pend_gtt))) {
             if (!release_down()) {
               ok = false;
               continue;
             }
           }
           if (w.gtt != ready_gtt) {
-            if (npend == 0 && ld_acquire(p.done + w.gtt) >= p.ph[0].n_mb) {
+            if (npend == 0 && tile_done(w.gtt)) {
               asm volatile("fence.proxy.async.global;" ::: "memory");
               ready_gtt = w.gtt;
             } else {
@@ -637,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
               ptx::bulk_load(st + C::kSfAOff + a * 2048, ph.sfw + sf_atoms(ph, w.e * ph.planes + a, w.mb, k), 2048,
                              &full[stage], pol_w);
           }
+          if (MODE == 2 && !dep_ready && rows_seen()) release_pending();  // the rows just became valid
           if (dep_ready) {
             load_b(ph, stage, k, row0, false);
           } else {
@@ -652,12 +713,60 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
           }
         }
       }
+      reinterpret_cast<volatile int*>(s_flags)[4] = 1;  // every unit issued: the watcher may stop
       if (!ok) {
         // unwinding: let the copies already in flight land before the CTA exits
         for (int i = 0; i < C::kStages && i < issued; ++i) {
           const uint32_t par = (i < stage) ? phase : (phase ^ 1u);
           wait_bar(&full[i], par, nullptr, 11, kDrainNs);
         }
+      }
+    }
+  } else if (warp == kWatchWarp) {
+    // ------------------------------------------------------------ token-tile watcher (fused launch)
+    // First the routing kernel's rows flag (when the launch polls flags), then
+    // lane l polls the completion counters of token tiles l, l + 32, ...: up
+    // to four not yet seen complete per round, their loads in flight together,
+    // and sets the bit of each tile whose gate/up row blocks are all done.
+    // Stops once the rows and every tile are seen complete, the producer has
+    // finished, or the launch aborts; anything it never sees ends in the
+    // producer's own bounded wait.
+    if (MODE == 2) {
+      const int target = p.ph[0].n_mb;
+      const volatile int* producer_done = s_flags + 4;
+      bool rows = p.ready == nullptr;  // without routing flags the rows were valid at launch
+      if (rows && lane == 0) smem_or_release(s_rows, 1u);
+      const uint64_t t0 = ptx::globaltimer();
+      for (uint32_t it = 0;; ++it) {
+        int tj[4], tv[4], cnt = 0;
+        bool more = false;
+        if (!rows) {
+          if (lane == 0 && ld_acquire(p.ready + 1) >= 1) smem_or_release(s_rows, 1u);
+          rows = __shfl_sync(kFullMask, static_cast<int>(smem_ld_acquire(s_rows)), 0) != 0;
+          more = !rows;
+        }
+        for (int j = lane; watch && j < n_tt; j += 32) {
+          if ((s_tile_done[j >> 5] >> (j & 31)) & 1u) continue;  // only this lane sets tile j's bit
+          if (cnt == 4) {
+            more = true;
+            break;
+          }
+          tj[cnt++] = j;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < cnt) tv[i] = ld_acquire(p.done + tj[i]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (i < cnt) {
+            if (tv[i] >= target) smem_or_release(&s_tile_done[tj[i] >> 5], 1u << (tj[i] & 31));
+            else more = true;
+          }
+        }
+        if (!__any_sync(kFullMask, more)) break;  // the rows and every tile seen complete
+        if (*producer_done || *abort_flag) break;
+        if (ptx::globaltimer() - t0 > kTimeoutNs) break;
+        __nanosleep(128);
       }
     }
   } else if (warp == 1) {
@@ -674,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
         if (wait_bar(&qfull[slot], (seq / kQueue) & 1, abort_flag, 6, kTimeoutNs)) u = s_queue[slot];
         ptx::mbar_arrive(&qempty[slot]);
         if (u < 0) break;
-        const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
+        const Unit w = decode(u);
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
         const int nacc = kind == 0 ? 2 : 1;
@@ -783,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(const __grid_cons
       ptx::named_bar_sync(bar_id, 128);
       if (u < 0) break;
       ptx::tc_fence_after();
-      const Unit w = decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0);
+      const Unit w = decode(u);
       const PhaseParams& ph = p.ph[w.phase];
       const int kind = unit_kind<MODE>(w.phase);
       const int nacc = kind == 0 ? 2 : 1;
@@ -1564,7 +1673,7 @@ cudaError_t launch_mode_bn(const GemmParams& prm, int grid, cudaStream_t stream,
   });
   if (attr_err != cudaSuccess) return attr_err;
   const cudaError_t err =
-      launch_kernel(moe_gemm_kernel<MODE, BN, FP4>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, pdl, prm);
+      launch_kernel(moe_gemm_kernel<MODE, BN, FP4>, dim3(grid), dim3(kGemmThreads), C::kSmemBytes, stream, pdl, prm);
   ++launch_counter();
   return err;
 }
@@ -1918,7 +2027,8 @@ cudaError_t launch_fused_experts(const GemmPlan& gate_up, const GemmPlan& down, 
 cudaError_t launch_fused_experts_fp4(const GemmPlan& gate_up, const GemmPlan& down, const Nvfp4Experts& wt,
                                      const uint8_t* xq, const uint8_t* xsf, float x_scale, const int32_t* offsets,
                                      int rows, int E, int H, int F, uint8_t* act_q, uint8_t* act_sf, float act_scale,
-                                     uint16_t* y_perm, void* scratch, int num_sms, cudaStream_t stream, bool pdl) {
+                                     uint16_t* y_perm, void* scratch, int num_sms, cudaStream_t stream, bool pdl,
+                                     const int* ready) {
   if (!fused_experts_supported(gate_up, down) || gate_up.bn > 32) return cudaErrorInvalidValue;
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -1939,7 +2049,7 @@ cudaError_t launch_fused_experts_fp4(const GemmPlan& gate_up, const GemmPlan& do
   prm.E = E;
   prm.rows = rows;
   prm.max_token_tiles = gate_up.max_token_tiles;
-  prm.ready = nullptr;
+  prm.ready = ready;
   return gate_up.bn == 16 ? launch_mode_bn<2, 16, true>(prm, num_sms, stream, pdl)
                           : launch_mode_bn<2, 32, true>(prm, num_sms, stream, pdl);
 }

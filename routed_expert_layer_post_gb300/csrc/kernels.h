@@ -55,6 +55,9 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 // the stream zeroed them): [0] the blocks' ticket (left zero), [1] set once
 // offsets, permutation and the cleared scratch are valid, [2] set once the
 // permuted rows are valid (the fused experts launch polls [1] and [2]).
+// With `xq` set the permuted rows are written as NVFP4 (codes [rows][H/2] to
+// `xq`, scale slots [rows][H/64][16] to `xsf`, FP32 scale g_in) instead of
+// bf16 to `x_perm`.
 constexpr int kRouteSyncInts = 4;
 bool route_decode_supported(int T, int H, int E, int G, int K);
 cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint16_t* w_post, const uint16_t* w_pre,
@@ -62,7 +65,8 @@ cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint
                                 float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
                                 int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
                                 uint16_t* x_perm, int* sync, void* clear, size_t clear_bytes, int num_sms,
-                                cudaStream_t stream, bool pdl, bool sync_zeroed = false);
+                                cudaStream_t stream, bool pdl, bool sync_zeroed = false, uint8_t* xq = nullptr,
+                                uint8_t* xsf = nullptr, float g_in = 0.f);
 
 // ---- permutation (permute.cu)
 size_t permute_scratch_bytes(int T, int K, int E);
@@ -136,7 +140,8 @@ cudaError_t launch_quantize_rows(const uint16_t* x, int rows, int K, float g, ui
 cudaError_t launch_fused_experts_fp4(const GemmPlan& gate_up, const GemmPlan& down, const Nvfp4Experts& wt,
                                      const uint8_t* xq, const uint8_t* xsf, float x_scale, const int32_t* offsets,
                                      int rows, int E, int H, int F, uint8_t* act_q, uint8_t* act_sf, float act_scale,
-                                     uint16_t* y_perm, void* scratch, int num_sms, cudaStream_t stream, bool pdl);
+                                     uint16_t* y_perm, void* scratch, int num_sms, cudaStream_t stream, bool pdl,
+                                     const int* ready = nullptr);
 // `err_out` (optional, device-visible): receives the device error word once
 // the expert launch before the combine has completed.
 cudaError_t launch_combine(const uint16_t* y_perm, const float* w, const int32_t* inv_perm, int T, int K, int H,

@@ -18,12 +18,16 @@
 // tickets, raises the first ready flag (offsets and scratch valid), copies the
 // permuted rows from the z it holds in registers and raises the second (rows
 // valid). The experts launch that follows polls those flags instead of waiting
-// for this kernel to end. Only the last block writes h': h' may alias h, and
+// for this kernel to end. With NVFP4 experts the permuted rows are written
+// quantized instead (E2M1 codes and E4M3 block scales under the FP32 input
+// scale, the same arithmetic as the standalone quantizer: TokenSpeed blog,
+// "TensorRT-LLM NVFP4 MoE", input quantization does not depend on routing). Only the last block writes h': h' may alias h, and
 // by then every block has read h. Ticket and flags are zeroed by the host
 // before the launch; the ticket is left zero.
 #include "common.cuh"
 #include "kernels.h"
 #include "norm_math.cuh"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace beam {
@@ -114,6 +118,31 @@ __device__ __forceinline__ void topk_block_phase2(int q, int gi, int TG, int K, 
   }
 }
 
+// One thread's 8 values (chunk c of a row) of an NVFP4 row: 16-value blocks
+// are chunk pairs (c, c + 1), and the four scales of a 64-value slot come
+// from chunks 8j .. 8j + 7 (lanes 8i .. 8i + 7 of a warp, since a warp's
+// chunks are 32-aligned). Codes two per byte, element 2i in the low nibble.
+// Every lane of the warp calls it.
+__device__ __forceinline__ void store_row_fp4(const uint4& v, float g, int c, uint8_t* q_row, uint4* sf_row) {
+  float f[8];
+  unpack8(v, f);
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
+  a = fmaxf(a, __shfl_xor_sync(kFullMask, a, 1));
+  float d;
+  const uint32_t sc = block_scale(a, g, &d);
+  uint32_t word = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) word |= e2m1_code(f[i], d) << (4 * i);
+  reinterpret_cast<uint32_t*>(q_row)[c] = word;
+  // scale byte of block c / 2 at byte (c % 8) / 2 of slot c / 8
+  uint32_t sw = (c & 1) ? 0u : sc << (8 * ((c & 7) >> 1));
+  sw |= __shfl_xor_sync(kFullMask, sw, 2);
+  sw |= __shfl_xor_sync(kFullMask, sw, 4);
+  if ((c & 7) == 0) sf_row[c >> 3] = make_uint4(sw, 0u, 0u, 0u);
+}
+
 // TMAX: token capacity of the register arrays
 template <int TMAX>
 __global__ void __launch_bounds__(kMaxThreads, 1)
@@ -123,7 +152,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                         uint4* h_out, uint4* __restrict__ z_out, float* __restrict__ logits,
                         int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_perm, uint4* __restrict__ x_perm,
-                        int* sync, int* __restrict__ clear, int clear_ints) {
+                        uint8_t* __restrict__ xq, uint4* __restrict__ xsf, float g_in, int* sync,
+                        int* __restrict__ clear, int clear_ints) {
   __shared__ F2 red[33];
   __shared__ float fred[32], fred2[32];
   __shared__ int hist[256];
@@ -304,7 +334,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   // barrier orders every thread's stores before thread 0's release)
   __syncthreads();
   if (c == 0) red_release(sync + 1, 1);
-  // permuted rows straight from the z this block holds
+  // permuted rows straight from the z this block holds (bf16, or NVFP4 codes and scales)
   for (int i = 0; i < pairs; ++i) {
     if (s_pos[i] < 0) continue;
     const int t = i / K;
@@ -312,7 +342,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 #pragma unroll
     for (int tt = 1; tt < TMAX; ++tt)
       if (tt == t) v = zc[tt];
-    x_perm[static_cast<size_t>(s_pos[i]) * nc + c] = v;
+    if (xq != nullptr)
+      store_row_fp4(v, g_in, c, xq + static_cast<size_t>(s_pos[i]) * nc * 4, xsf + static_cast<size_t>(s_pos[i]) * (nc / 8));
+    else
+      x_perm[static_cast<size_t>(s_pos[i]) * nc + c] = v;
   }
   __syncthreads();
   if (c == 0) {
@@ -337,7 +370,8 @@ cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint
                                 float scale, float eps, int n, uint16_t* h_out, uint16_t* z_out, float* logits,
                                 int32_t* ids, float* w, int32_t* offsets, int32_t* perm_token, int32_t* inv_perm,
                                 uint16_t* x_perm, int* sync, void* clear, size_t clear_bytes, int num_sms,
-                                cudaStream_t stream, bool pdl, bool sync_zeroed) {
+                                cudaStream_t stream, bool pdl, bool sync_zeroed, uint8_t* xq, uint8_t* xsf,
+                                float g_in) {
   cudaError_t err = cudaSuccess;
   if (!sync_zeroed && (err = cudaMemsetAsync(sync, 0, kRouteSyncInts * sizeof(int), stream)) != cudaSuccess)
     return err;
@@ -349,8 +383,9 @@ cudaError_t launch_route_decode(const uint16_t* h, const uint16_t* x, const uint
                       reinterpret_cast<const uint4*>(h),
                       reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(w_post),
                       reinterpret_cast<const uint4*>(w_pre), W, bias, T, E, G, TG, K, scale, inv_h, eps, coef, reinterpret_cast<uint4*>(h_out), reinterpret_cast<uint4*>(z_out),
-                      logits, ids, w, offsets, perm_token, inv_perm, reinterpret_cast<uint4*>(x_perm), sync,
-                      static_cast<int*>(clear), static_cast<int>(clear_bytes / sizeof(int)));
+                      logits, ids, w, offsets, perm_token, inv_perm, reinterpret_cast<uint4*>(x_perm), xq,
+                      reinterpret_cast<uint4*>(xsf), g_in, sync, static_cast<int*>(clear),
+                      static_cast<int>(clear_bytes / sizeof(int)));
   ++launch_counter();
   return err;
 }

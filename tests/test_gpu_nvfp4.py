@@ -225,3 +225,29 @@ def test_layer_nvfp4_matches_oracle(name, tokens):
     mx, rel = layer_errors(f64_of(y)[tokens][same], ref["y"][same])
     print(f"{name} NVFP4 layer: tokens {tokens.size}, max|dy| {mx:.3e}, rel-L2 {rel:.3e}")
     assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
+
+
+_FP4_EXPERTS = {}
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_decode_routing_writes_rows_like_the_quantizer(T):
+    """At decode sizes the routing kernel writes the permuted rows as NVFP4
+    itself. The layer output must be bit-identical to the experts stage fed
+    with the same routing and the standalone row quantizer."""
+    beam = beam_module()
+    m = model("decode_t64")
+    cfg = m.cfg.with_(T=T)
+    mc = beam.make_config(cfg.H, cfg.E, cfg.G, cfg.TG, cfg.K, cfg.F, cfg.routed_scale, cfg.eps)
+    if "beam" not in _FP4_EXPERTS:
+        _FP4_EXPERTS["beam"] = beam.beam_nvfp4_quantize_experts(m.dev[0], m.dev[1], mc)
+    wt = beam.nvfp4_weights_struct(dev_bf16(m.wp_bits), dev_bf16(m.wq_bits), torch.from_numpy(m.W_r).cuda(),
+                                   torch.from_numpy(m.bias).cuda(), _FP4_EXPERTS["beam"], G_IN, G_ACT)
+    hb, xb = make_activations(cfg)
+    _, y, dbg = beam.beam_moe_layer_nvfp4(dev_bf16(hb), dev_bf16(xb), cfg.n, wt, mc, debug=True)
+    offsets, _, inv, x_perm = beam.beam_moe_permute(dbg["topk_ids"], dbg["z"], mc)
+    y2, _ = beam.beam_moe_experts_nvfp4(x_perm, offsets, wt, dbg["topk_w"], inv, mc, T)
+    torch.cuda.synchronize()
+    assert beam.beam_get_device_error() == 0
+    assert torch.equal(offsets, dbg["expert_offsets"])
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
