@@ -56,7 +56,14 @@ constexpr int kThreads = 320;
 // full HBM load one takes several microseconds) to learn that a down unit's
 // rows are complete.
 constexpr int kWatchWarp = kThreads / 32;
-constexpr int kGemmThreads = kThreads + 32;
+// ... and a claim warp (warp 11), which takes unit ids from the launch's
+// counter two units ahead of the producer and hands them over in shared
+// memory: the atomic's round trip then overlaps two units' loads without the
+// producer ever waiting on it (an NVFP4 unit's loads take about as long as
+// that round trip under full HBM load).
+constexpr int kClaimWarp = kWatchWarp + 1;
+constexpr int kClaimDepth = 2;
+constexpr int kGemmThreads = kThreads + 64;
 constexpr int kMaxWatchTiles = 2048;  // token tiles the shared-memory mirror holds (one bit each)
 constexpr int kEpiGroups = 2;
 constexpr int kBM = 128;                     // weight rows per tile (MMA M)
@@ -244,18 +251,22 @@ __device__ __forceinline__ int tile_owner(int j, int E, const int* s_ttstart) {
 // Tiles of a phase are laid out expert by expert, row block by row block,
 // token tile fastest; expert e's tiles start at n_mb * s_ttstart[e].
 // `rot0` (fused launch): phase-0 tiles are taken starting at tile rot0 (an
-// expert boundary), wrapping around at n_tiles0.
+// expert boundary), wrapping around at n_tiles0; with `rot_down` the phase-1
+// tiles are rotated to the same expert.
 __device__ __forceinline__ Unit decode_unit(int u, int n_units0, const GemmParams& p, const int* s_ttstart,
-                                            const int* s_ntt, int rot0 = 0, int n_tiles0 = 0) {
+                                            const int* s_ntt, int rot0 = 0, int n_tiles0 = 0,
+                                            bool rot_down = false) {
   Unit r;
   r.phase = (u < n_units0) ? 0 : 1;
   const PhaseParams& ph = p.ph[r.phase];
   const int v = r.phase == 0 ? u : u - n_units0;
   r.tile = v / ph.split;
   r.s = v - r.tile * ph.split;
-  if (r.phase == 0 && rot0 != 0) {
-    r.tile += rot0;
-    if (r.tile >= n_tiles0) r.tile -= n_tiles0;
+  if (rot0 != 0 && (r.phase == 0 || rot_down)) {
+    const int rt = (rot0 / p.ph[0].n_mb) * ph.n_mb;      // the same first token tile
+    const int nt = (n_tiles0 / p.ph[0].n_mb) * ph.n_mb;  // this phase's tiles
+    r.tile += rt;
+    if (r.tile >= nt) r.tile -= nt;
   }
   const int q = r.tile / ph.n_mb;
   r.e = tile_owner(q, p.E, s_ttstart);
@@ -332,7 +343,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   uint64_t* qfull = tempty + 4;
   uint64_t* qempty = qfull + kQueue;
   uint64_t* drain = qempty + kQueue;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* cfull = drain + 1;          // a claimed unit id is in the slot
+  uint64_t* cfree = cfull + kClaimDepth;  // the producer has taken it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cfree + kClaimDepth);
   // [0] abort; [2] routing flags never came; [4] the producer has finished;
   // [6] the routing rows flag was seen; per epilogue group g: [4g+1] last
   // arriver, [4g+3] current unit
@@ -343,6 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   int* s_ttstart = s_ntt + kMaxE;
   uint32_t* s_tile_done = reinterpret_cast<uint32_t*>(s_ttstart + kMaxE + 1);  // MODE 2: watcher bits
   uint32_t* s_rows = reinterpret_cast<uint32_t*>(s_flags + 6);  // MODE 2: the routing rows flag was seen
+  int* s_claim = reinterpret_cast<int*>(s_tile_done + kMaxWatchTiles / 32);  // claimed unit ids
   volatile int* abort_flag = s_flags;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -360,6 +374,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       ptx::mbar_init(&qempty[q], 2);  // released by the MMA thread and the epilogue leader
     }
     ptx::mbar_init(drain, 1);
+    for (int c = 0; c < kClaimDepth; ++c) {
+      ptx::mbar_init(&cfull[c], 1);
+      ptx::mbar_init(&cfree[c], 1);
+    }
     for (int i = 0; i < 8; ++i) s_flags[i] = 0;
     ptx::fence_mbar_init();
   }
@@ -374,6 +392,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       ptx::prefetch_tensormap(&p.ph[0].tmap_sfx);
       ptx::prefetch_tensormap(&p.ph[1].tmap_sfx);
     }
+  }
+  if (warp == kWatchWarp && lane == 0) {
+    // Touch the launch's scalar parameters now, while the previous kernel
+    // runs: every role reads them right after the dependency resolves, and a
+    // constant-cache miss then costs a global round trip on the path to the
+    // first weight load.
+    uint32_t sink = static_cast<uint32_t>(p.E + p.rows + p.max_token_tiles) ^
+                    static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.offsets) ^
+                                          reinterpret_cast<uintptr_t>(p.counter) ^ reinterpret_cast<uintptr_t>(p.done) ^
+                                          reinterpret_cast<uintptr_t>(p.ready));
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const PhaseParams& q = p.ph[i];
+      sink += static_cast<uint32_t>(q.n_mb + q.ksteps + q.split + q.out_ld + q.planes + q.max_tiles) ^
+              static_cast<uint32_t>(reinterpret_cast<uintptr_t>(q.out) ^ reinterpret_cast<uintptr_t>(q.out_q) ^
+                                    reinterpret_cast<uintptr_t>(q.out_sf) ^ reinterpret_cast<uintptr_t>(q.sfw) ^
+                                    reinterpret_cast<uintptr_t>(q.wscale) ^ reinterpret_cast<uintptr_t>(q.partials) ^
+                                    reinterpret_cast<uintptr_t>(q.tickets)) ^
+              __float_as_uint(q.xscale) ^ __float_as_uint(q.out_scale);
+    }
+    asm volatile("" ::"r"(sink));
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, C::kTmemCols);
@@ -460,11 +499,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   // Their epilogues run first on every SM, with cold instructions under full
   // HBM load, and finish late; the down units of those experts come last, so
   // nothing waits on them. rot0 is the start of the earliest expert such that
-  // the experts from it to the end hold at least one wave of units. (Handing
-  // each token tile's down units out a few tiles after its gate/up units,
-  // interleaved with the later gate/up units, measured slower: 1.28 against
-  // 1.01 ms at 64 tokens with NVFP4 experts, 128 against 122 us at one token
-  // in bf16.)
+  // the experts from it to the end hold at least one wave of units. With
+  // NVFP4 experts (a quarter of the bytes per unit, so the first wave's
+  // epilogues are not late) the down units follow the gate/up order instead:
+  // one token 83.4 -> 81.3 us per layer; in bf16 that order measured 1 %
+  // slower at one token. (Handing each token tile's down units out a few
+  // tiles after its gate/up units, interleaved with the later gate/up units,
+  // measured slower: 1.28 against 1.01 ms at 64 tokens with NVFP4 experts,
+  // 128 against 122 us at one token in bf16.)
   int rot0 = 0;
   if (MODE == 2 && n_tiles0 > 0) {
     const int wave_tiles = (static_cast<int>(gridDim.x) + p.ph[0].split - 1) / p.ph[0].split;
@@ -476,7 +518,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     const int n_tiles1 = n_tt * p.ph[1].n_mb;
     if (n_tiles1 <= p.ph[1].max_tiles) n_units += n_tiles1 * p.ph[1].split;
   }
-  auto decode = [&](int u) -> Unit { return decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0); };
+  auto decode = [&](int u) -> Unit { return decode_unit(u, n_units0, p, s_ttstart, s_ntt, rot0, n_tiles0, FP4); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler + TMA producer
@@ -582,9 +624,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         ready_gtt = pend_gtt;
         return true;
       };
-      int u_next = u_first;
       for (int seq = 0;; ++seq) {
-        int u = u_next;
+        // unit ids: the first from the set-up, then from the claim warp
+        int u = u_first;
+        if (seq > 0) {
+          const int c = (seq - 1) % kClaimDepth;
+          u = -1;
+          if (ok && wait_bar(&cfull[c], ((seq - 1) / kClaimDepth) & 1, abort_flag, 14, kTimeoutNs)) {
+            u = *reinterpret_cast<volatile int*>(&s_claim[c]);
+            ptx::mbar_arrive(&cfree[c]);
+          }
+        }
         if (u >= n_units || !ok) u = -1;
         if (u < 0 && !dep_ready) release_pending();
         if (MODE == 2 && npend > 0 && ok && (u < 0 || seq - pend_seq0 >= kQueue - 1)) {
@@ -609,8 +659,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           ptx::mbar_arrive(&qfull[s2]);
           break;
         }
-        // ask for the following unit now: the atomic's round trip overlaps this unit's loads
-        u_next = atomicAdd(p.counter, 1);
         const Unit w = decode(u);
         const PhaseParams& ph = p.ph[w.phase];
         const int kind = unit_kind<MODE>(w.phase);
@@ -720,6 +768,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           const uint32_t par = (i < stage) ? phase : (phase ^ 1u);
           wait_bar(&full[i], par, nullptr, 11, kDrainNs);
         }
+      }
+    }
+  } else if (warp == kClaimWarp) {
+    // ------------------------------------------------------------ unit claims
+    // The producer took the first id in the set-up; every further id comes
+    // from here, at most kClaimDepth ahead of the producer. Stops after
+    // handing over an id past the end, or once the producer has finished or
+    // the launch aborts.
+    if (lane == 0) {
+      const volatile int* producer_done = s_flags + 4;
+      for (int i = 0;; ++i) {
+        const int c = i % kClaimDepth;
+        const uint32_t addr = ptx::smem_u32(&cfree[c]);
+        const uint32_t par = ((i / kClaimDepth) & 1) ^ 1u;
+        bool free_slot = ptx::mbar_try_wait(addr, par);
+        const uint64_t t0 = free_slot ? 0 : ptx::globaltimer();
+        while (!free_slot) {
+          if (*producer_done || *abort_flag || ptx::globaltimer() - t0 > kTimeoutNs) break;
+          __nanosleep(32);
+          free_slot = ptx::mbar_try_wait(addr, par);
+        }
+        if (!free_slot) break;
+        const int u = atomicAdd(p.counter, 1);
+        *reinterpret_cast<volatile int*>(&s_claim[c]) = u;
+        ptx::mbar_arrive(&cfull[c]);
+        if (u >= n_units) break;
       }
     }
   } else if (warp == kWatchWarp) {
@@ -1051,9 +1125,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
 // pair's bytes, so the leader issues a stage's MMAs with no extra hop.
 //
 // Gate/up: a CTA's 128 weight rows are 64 gate rows and the up rows of the
-// same 64 d_ff columns (two 64-row TMA boxes), so its accumulator holds gate
-// in tensor-memory lanes 0-63 and up in lanes 64-127; the epilogue pairs them
-// through shared memory for SwiGLU. A pair covers 128 d_ff columns. Down: 128
+// same 64 d_ff columns (one TMA box of 64 rows in both planes), so its
+// accumulator holds gate in tensor-memory lanes 0-63 and up in lanes 64-127;
+// the epilogue pairs them through shared memory for SwiGLU. A pair covers 128 d_ff columns. Down: 128
 // rows of W_d per CTA, 256 per pair.
 //
 // Narrow last tiles: an expert's rows rarely fill its last 256-token tile
@@ -1259,8 +1333,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (leader) ptx::mbar_arrive_expect_tx(&full[stage], stage_tx);
           if (MODE == 0) {
             const int f0 = w.mb * kBM + static_cast<int>(rank) * 64;
-            ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, f0, 2 * w.e, pol_w);                    // gate rows
-            ptx::tma_load_3d_pair(st + kTileABytes / 2, &ph.tmap_w, fb, k * kBK, f0, 2 * w.e + 1, pol_w);  // up
+            // one box of both planes: the 64 gate rows, then the same 64 d_ff columns' up rows
+            ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, f0, 2 * w.e, pol_w);
           } else {
             ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, w.mb * 2 * kBM + static_cast<int>(rank) * kBM, w.e,
                                   pol_w);
@@ -1921,12 +1995,15 @@ cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* 
   const int planes = mode == 0 ? 2 : 1;
   const int prows = mode == 0 ? F : H;
   {
-    // gate/up: 64-row boxes (a CTA's 64 gate rows and the matching 64 up rows); down: 128 rows
+    // gate/up: a box of 64 rows in both planes (a CTA's 64 gate rows and the
+    // matching 64 up rows, one TMA instruction: the producer's issue rate is
+    // part of what feeds the MMAs); down: 128 rows
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kdim), static_cast<cuuint64_t>(prows),
                                 static_cast<cuuint64_t>(E) * planes};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kdim) * 2,
                                    static_cast<cuuint64_t>(kdim) * 2 * static_cast<cuuint64_t>(prows)};
-    const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(mode == 0 ? 64 : kBM), 1};
+    const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(mode == 0 ? 64 : kBM),
+                               static_cast<cuuint32_t>(mode == 0 ? 2 : 1)};
     if (!encode_map(&ph.tmap_w, weights, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
