@@ -593,10 +593,12 @@ def measure(run, args, env, world):
     floor["peak_source"] = peaks_kind
 
     # end to end through the host-buffer entry point: H2D of h, x and D2H of h', y inside the timed region
-    # (the host-buffer entry point takes bf16 experts: no end-to-end number for NVFP4)
     e2e = None
-    if not args.no_e2e and not fp4:
-        hbytes = lib.beam_moe_layer_host_workspace_size(ctypes.byref(mc), T)
+    host_fn = lib.beam_moe_layer_nvfp4_host if fp4 else lib.beam_moe_layer_host
+    host_name = "beam_moe_layer_nvfp4_host" if fp4 else "beam_moe_layer_host"
+    if not args.no_e2e:
+        hbytes = (lib.beam_moe_layer_nvfp4_host_workspace_size if fp4 else
+                  lib.beam_moe_layer_host_workspace_size)(ctypes.byref(mc), T)
         ws_h = torch.empty(hbytes, dtype=torch.uint8, device=device)
         ho = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
         yo = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
@@ -613,18 +615,17 @@ def measure(run, args, env, world):
             flush_l2()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            st = lib.beam_moe_layer_host(hi.data_ptr(), xi.data_ptr(), cfg.n,
-                                         ctypes.byref(weights), T, ctypes.byref(mc), ho.data_ptr(), yo.data_ptr(),
-                                         ws_h.data_ptr(), hbytes, sp)
+            st = host_fn(hi.data_ptr(), xi.data_ptr(), cfg.n, ctypes.byref(weights), T, ctypes.byref(mc),
+                         ho.data_ptr(), yo.data_ptr(), ws_h.data_ptr(), hbytes, sp)
             dt = time.perf_counter() - t0
             if st != 0:
-                raise RuntimeError(f"beam_moe_layer_host ({name}): {beam.beam_status_string(st)}")
+                raise RuntimeError(f"{host_name} ({name}): {beam.beam_status_string(st)}")
             if i >= 3:
                 tot += dt
         tot = reduce_max(tot, device)
         e2e = {"value": T * Ke * world / tot, "unit": UNIT, "h2d_bytes_per_step": 2 * T * H * 2,
                "d2h_bytes_per_step": 2 * T * H * 2, "steps": Ke, "us_per_layer": 1e6 * tot / Ke,
-               "timing": "host clock around beam_moe_layer_host (returns after a stream synchronise); the same "
+               "timing": f"host clock around {host_name} (returns after a stream synchronise); the same "
                          "page-locked h, x, h', y buffers every step, refilled with the step's batch before the "
                          "timed call"}
         del ws_h

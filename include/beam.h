@@ -337,7 +337,11 @@ beam_status_t beam_moe_layer_nvfp4(const uint16_t* h, const uint16_t* x, int n,
  * from the mapped memory and the layer writes h_out and y_out to it directly
  * instead of four copy-engine transfers; the results are the same bits. h_out
  * must not alias x; y_out must alias none of the others. Weights stay device
- * pointers. Workspace: beam_moe_layer_host_workspace_size.
+ * pointers. Workspace: beam_moe_layer_host_workspace_size. From 8192 tokens
+ * (bf16 experts, Beam-size router) the layer runs pipelined with the copies:
+ * the tokens are copied in four chunks, each chunk's boundary, router and
+ * top-k start once its copy has landed, and the combine and the copy of y back
+ * go chunk by chunk; the results are the same bits.
  * Repeated calls on that mapped-memory path: the second call with the same
  * device, buffers, n, T, weights, config and workspace captures its launches
  * into a CUDA graph, and later calls with the same arguments replay it (one
@@ -355,6 +359,16 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
                                   const beam_moe_weights_t* weights, int T,
                                   const beam_moe_config_t* cfg, uint16_t* h_out_host,
                                   uint16_t* y_out_host, void* ws, size_t ws_bytes, void* stream);
+
+/* beam_moe_layer_host with NVFP4 experts (the layer of beam_moe_layer_nvfp4):
+ * the same host-buffer rules, mapped-memory path and graph replays.
+ * Workspace: beam_moe_layer_nvfp4_host_workspace_size (0 for shapes the
+ * NVFP4 experts do not support). */
+size_t beam_moe_layer_nvfp4_host_workspace_size(const beam_moe_config_t* cfg, int T);
+beam_status_t beam_moe_layer_nvfp4_host(const uint16_t* h_host, const uint16_t* x_host, int n,
+                                        const beam_moe_nvfp4_weights_t* weights, int T,
+                                        const beam_moe_config_t* cfg, uint16_t* h_out_host,
+                                        uint16_t* y_out_host, void* ws, size_t ws_bytes, void* stream);
 
 /* Frees every graph that beam_moe_layer_host has captured (their memory
  * only: a captured graph runs only when a call repeats its exact arguments,

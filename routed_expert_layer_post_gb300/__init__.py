@@ -29,7 +29,8 @@ __all__ = [
     "beam_get_device_error", "beam_check_bounded_wait", "beam_check_bounded_wait_pending",
     "beam_release_host_graphs", "MoeNvfp4Weights", "MoeNvfp4Intermediates", "Nvfp4Experts",
     "beam_nvfp4_quantize_experts", "beam_nvfp4_quantize_rows", "nvfp4_weights_struct", "beam_moe_experts_nvfp4",
-    "beam_moe_layer_nvfp4", "beam_moe_nvfp4_workspace_size", "beam_last_launch_count", "beam_status_string", "Workspace",
+    "beam_moe_layer_nvfp4", "beam_moe_nvfp4_workspace_size", "beam_moe_layer_nvfp4_host",
+    "beam_moe_layer_nvfp4_host_workspace_size", "beam_last_launch_count", "beam_status_string", "Workspace",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libbeam.so")
@@ -110,6 +111,10 @@ _SIGNATURES = {
     "beam_moe_layer_host": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeWeights), c_int,
                                     ctypes.POINTER(MoeConfig), c_void_p, c_void_p, c_void_p, c_size_t,
                                     c_void_p]),
+    "beam_moe_layer_nvfp4_host_workspace_size": (c_size_t, [ctypes.POINTER(MoeConfig), c_int]),
+    "beam_moe_layer_nvfp4_host": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeNvfp4Weights), c_int,
+                                          ctypes.POINTER(MoeConfig), c_void_p, c_void_p, c_void_p, c_size_t,
+                                          c_void_p]),
     "beam_get_device_error": (c_int, [ctypes.POINTER(c_int), c_void_p]),
     "beam_check_bounded_wait": (c_int, [c_void_p, c_int, ctypes.POINTER(c_int), c_void_p]),
     "beam_check_bounded_wait_pending": (c_int, [c_void_p, c_int, c_void_p]),
@@ -394,6 +399,26 @@ def beam_moe_layer_host(h_host: torch.Tensor, x_host: torch.Tensor, n: int, weig
     y_out_host = torch.empty_like(h_host) if y_out_host is None else y_out_host
     buf = _ws(beam_moe_layer_host_workspace_size(cfg, T), ws)
     _check("beam_moe_layer_host", library().beam_moe_layer_host(
+        h_host.data_ptr(), x_host.data_ptr(), n, ctypes.byref(weights), T, ctypes.byref(cfg),
+        h_out_host.data_ptr(), y_out_host.data_ptr(), buf.data_ptr(), buf.numel(), _stream()))
+    return h_out_host, y_out_host
+
+
+def beam_moe_layer_nvfp4_host_workspace_size(cfg: MoeConfig, T: int) -> int:
+    return library().beam_moe_layer_nvfp4_host_workspace_size(ctypes.byref(cfg), T)
+
+
+def beam_moe_layer_nvfp4_host(h_host: torch.Tensor, x_host: torch.Tensor, n: int, weights: MoeNvfp4Weights,
+                              cfg: MoeConfig, h_out_host=None, y_out_host=None, ws: Optional[Workspace] = None):
+    """beam_moe_layer_host with NVFP4 experts."""
+    T = h_host.shape[0]
+    for t in (h_host, x_host):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise BeamError("beam_moe_layer_nvfp4_host expects contiguous bf16 host tensors")
+    h_out_host = torch.empty_like(h_host) if h_out_host is None else h_out_host
+    y_out_host = torch.empty_like(h_host) if y_out_host is None else y_out_host
+    buf = _ws(beam_moe_layer_nvfp4_host_workspace_size(cfg, T), ws)
+    _check("beam_moe_layer_nvfp4_host", library().beam_moe_layer_nvfp4_host(
         h_host.data_ptr(), x_host.data_ptr(), n, ctypes.byref(weights), T, ctypes.byref(cfg),
         h_out_host.data_ptr(), y_out_host.data_ptr(), buf.data_ptr(), buf.numel(), _stream()))
     return h_out_host, y_out_host

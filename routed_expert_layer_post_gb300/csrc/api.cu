@@ -710,6 +710,13 @@ size_t beam_moe_layer_host_workspace_size(const beam_moe_config_t* cfg, int T) {
   return base + 4 * act;
 }
 
+size_t beam_moe_layer_nvfp4_host_workspace_size(const beam_moe_config_t* cfg, int T) {
+  const size_t base = beam_moe_nvfp4_workspace_size(cfg, T);
+  if (base == 0 && T != 0) return 0;
+  const size_t act = align_up(static_cast<size_t>(T) * cfg->hidden * 2);
+  return base + 4 * act;
+}
+
 namespace {
 
 // Device-visible address of a page-locked host buffer, or nullptr.
@@ -777,6 +784,8 @@ struct HostCall {
   void* h_out;
   void* y_out;
   beam_moe_weights_t wt;
+  beam_moe_nvfp4_weights_t fp4w;  // with fp4: the NVFP4 experts (wt then holds the shared weights only)
+  int fp4;
   beam_moe_config_t cfg;
   void* ws;
   size_t ws_bytes;
@@ -810,7 +819,7 @@ beam_status_t zero_copy_launches(const HostCall& k, cudaStream_t s) {
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
   const beam_status_t st = layer_impl(d_h, d_x, k.n, &k.wt, k.T, &k.cfg, static_cast<uint16_t*>(k.h_out),
                                       static_cast<uint16_t*>(k.y_out), nullptr, lws, lws_bytes, s, route, nullptr,
-                                      k.err_out);
+                                      k.err_out, k.fp4 ? &k.fp4w : nullptr);
   launch_counter() += 1;
   return st;
 }
@@ -885,14 +894,19 @@ bool capture_graph(HostGraph* g) {
   return ok;
 }
 
-// The copy path's side stream and events, one set per device. From
+// The copy path's side streams and events, one set per device. From
 // kOverlapTokens tokens up, h' (final once the boundary has run) is copied
-// back on the side stream while the rest of the layer computes.
+// back on the side stream while the rest of the layer computes. From
+// kPipeTokens tokens up the layer is pipelined with the copies in
+// kPipeChunks token chunks (layer_host_pipelined).
 constexpr int kOverlapTokens = 64;
+constexpr int kPipeTokens = 8192;  // measured: 16384 tokens e2e 10.70 -> 10.39 ms; 2048 tokens 3.58 -> 3.69 ms (not used there)
+constexpr int kPipeChunks = 4;
 
 struct CopyAux {
-  cudaStream_t side = nullptr;
+  cudaStream_t side = nullptr, side_in = nullptr;
   cudaEvent_t after_boundary = nullptr, h_copied = nullptr;
+  cudaEvent_t in_done[kPipeChunks] = {}, bnd_done[kPipeChunks] = {}, y_done[kPipeChunks] = {};
   bool ok = false;
 };
 
@@ -902,9 +916,15 @@ CopyAux g_aux[64];
 CopyAux* copy_aux(int dev) {
   CopyAux& a = g_aux[dev];
   if (!a.ok) {
-    if (cudaStreamCreateWithFlags(&a.side, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a.after_boundary, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a.h_copied, cudaEventDisableTiming) != cudaSuccess) {
+    bool ok = cudaStreamCreateWithFlags(&a.side, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&a.side_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&a.after_boundary, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&a.h_copied, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; ok && c < kPipeChunks; ++c)
+      ok = cudaEventCreateWithFlags(&a.in_done[c], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&a.bnd_done[c], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&a.y_done[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
       cudaGetLastError();
       return nullptr;
     }
@@ -913,12 +933,109 @@ CopyAux* copy_aux(int dev) {
   return &a;
 }
 
-}  // namespace
+// Large batches through host buffers, pipelined with the copies: the
+// tokens arrive in kPipeChunks chunks on a copy-in stream, and each chunk's
+// boundary, router and top-k run (on the call's stream) while the next chunk
+// is still being copied; h' goes back on the side stream once the last
+// chunk's boundary has run. The permutation and the expert GEMMs take the
+// whole batch; the combine then runs chunk by chunk, each chunk's y copied
+// back while the next chunk combines. Every kernel computes each token as in
+// beam_moe_layer (the same kernels on the same per-token data; chunks hold
+// more than 128 tokens, so the router is the same tensor-core kernel), so
+// the outputs are bit-identical to it.
+beam_status_t layer_host_pipelined(const uint16_t* h_host, const uint16_t* x_host, int n,
+                                   const beam_moe_weights_t* wt, int T, const beam_moe_config_t* cfg,
+                                   uint16_t* h_out_host, uint16_t* y_out_host, uint16_t* d_h, uint16_t* d_x,
+                                   uint16_t* d_hn, uint16_t* d_y, char* base, int sms, cudaStream_t s, CopyAux* a,
+                                   int* err_slot) {
+  const int H = cfg->hidden, E = cfg->num_experts, K = cfg->topk;
+  const LayerWs L = layer_ws(cfg, T, sms);
+  uint16_t* z = reinterpret_cast<uint16_t*>(base + L.z);
+  float* logits = reinterpret_cast<float*>(base + L.logits);
+  int32_t* ids = reinterpret_cast<int32_t*>(base + L.ids);
+  float* w = reinterpret_cast<float*>(base + L.w);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  int32_t* inv = reinterpret_cast<int32_t*>(base + L.inv);
+  uint16_t* x_perm = reinterpret_cast<uint16_t*>(base + L.x_perm);
+  int* router_ticket = reinterpret_cast<int*>(base + L.router_ticket);
+  beam::GemmPlan p0, p1;
+  beam::plan_experts(T, K, E, H, cfg->d_ff, sms, &p0, &p1, false);
+  char* ews = base + L.experts;
+  const ExpertsWs xw = experts_ws(cfg, T, sms);
+  const uint16_t* y_perm = reinterpret_cast<const uint16_t*>(ews + xw.y_perm);
+  const size_t row = static_cast<size_t>(H) * 2;
+  auto t0 = [&](int c) { return static_cast<int>(static_cast<long long>(T) * c / kPipeChunks); };
+  cudaError_t e = cudaSuccess;
+  launch_counter() = 0;
+  // the copy-in stream starts after everything queued on the call's stream before this call
+  if ((e = cudaEventRecord(a->h_copied, s)) != cudaSuccess || (e = cudaStreamWaitEvent(a->side_in, a->h_copied, 0)) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  for (int c = 0; c < kPipeChunks; ++c) {
+    const size_t o = static_cast<size_t>(t0(c)) * H, bytes = static_cast<size_t>(t0(c + 1) - t0(c)) * row;
+    if (cudaMemcpyAsync(d_h + o, h_host + o, bytes, cudaMemcpyHostToDevice, a->side_in) != cudaSuccess ||
+        cudaMemcpyAsync(d_x + o, x_host + o, bytes, cudaMemcpyHostToDevice, a->side_in) != cudaSuccess ||
+        cudaEventRecord(a->in_done[c], a->side_in) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+  }
+  for (int c = 0; c < kPipeChunks; ++c) {
+    const int tc = t0(c + 1) - t0(c);
+    const size_t o = static_cast<size_t>(t0(c)) * H;
+    if (cudaStreamWaitEvent(s, a->in_done[c], 0) != cudaSuccess) return BEAM_ERR_CUDA;
+    e = beam::launch_boundary(d_h + o, d_x + o, wt->w_post, wt->w_pre, tc, H, cfg->eps, n, d_hn + o, z + o, s,
+                              /*pdl=*/false, c == 0 ? router_ticket : nullptr);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    if (c == kPipeChunks - 1) {
+      // h' goes back once the copies in are done: the link then carries it
+      // alongside the expert GEMMs instead of slowing the incoming chunks
+      if (cudaEventRecord(a->bnd_done[c], s) != cudaSuccess ||
+          cudaStreamWaitEvent(a->side, a->bnd_done[c], 0) != cudaSuccess ||
+          cudaMemcpyAsync(h_out_host, d_hn, static_cast<size_t>(T) * row, cudaMemcpyDeviceToHost, a->side) !=
+              cudaSuccess)
+        return BEAM_ERR_CUDA;
+    }
+    const size_t lo = static_cast<size_t>(t0(c)) * E, ko = static_cast<size_t>(t0(c)) * K;
+    e = beam::launch_router_tc(z + o, wt->router_w, tc, E, H, logits + lo,
+                               reinterpret_cast<uint16_t*>(base + L.router_w3), sms, s, true);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    e = beam::launch_topk(logits + lo, wt->bias, tc, E, cfg->num_groups, cfg->topk_groups, K, cfg->routed_scale,
+                          ids + ko, w + ko, s, true);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
+  // the permutation also zeroes the expert GEMMs' counters and tickets
+  e = beam::launch_permute(ids, z, T, K, E, H, offsets, perm, inv, x_perm, base + L.perm_scratch, s, true,
+                           ews + xw.gemm, beam::gemm_clear_bytes(p0, p1));
+  if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  const int launches = launch_counter();
+  launch_counter() = 0;
+  beam_status_t st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, nullptr, ews, sms, s,
+                                 nullptr, true, /*cleared=*/true, nullptr, nullptr);
+  if (st != BEAM_OK) return st;
+  for (int c = 0; c < kPipeChunks; ++c) {
+    const int tc = t0(c + 1) - t0(c);
+    const size_t o = static_cast<size_t>(t0(c)) * H, ko = static_cast<size_t>(t0(c)) * K;
+    e = beam::launch_combine(y_perm, w + ko, inv + ko, tc, K, H, d_y + o, s, /*pdl=*/true,
+                             c == 0 ? err_slot : nullptr);
+    if (e != cudaSuccess || cudaEventRecord(a->y_done[c], s) != cudaSuccess ||
+        cudaStreamWaitEvent(a->side_in, a->y_done[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(y_out_host + o, d_y + o, static_cast<size_t>(tc) * row, cudaMemcpyDeviceToHost,
+                        a->side_in) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+  }
+  launch_counter() += launches;
+  // the call's stream ends after both side streams' copies
+  if (cudaEventRecord(a->after_boundary, a->side) != cudaSuccess ||
+      cudaStreamWaitEvent(s, a->after_boundary, 0) != cudaSuccess ||
+      cudaEventRecord(a->h_copied, a->side_in) != cudaSuccess || cudaStreamWaitEvent(s, a->h_copied, 0) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  return BEAM_OK;
+}
 
-beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
-                                  const beam_moe_weights_t* wt, int T, const beam_moe_config_t* cfg,
-                                  uint16_t* h_out_host, uint16_t* y_out_host, void* ws, size_t ws_bytes,
-                                  void* stream) {
+// beam_moe_layer_host and beam_moe_layer_nvfp4_host: `fp4w` set for NVFP4
+// experts (then `wt` holds the shared weights only).
+beam_status_t layer_host_impl(const uint16_t* h_host, const uint16_t* x_host, int n, const beam_moe_weights_t* wt,
+                              const beam_moe_nvfp4_weights_t* fp4w, int T, const beam_moe_config_t* cfg,
+                              uint16_t* h_out_host, uint16_t* y_out_host, void* ws, size_t ws_bytes, void* stream) {
   beam_status_t st = check_config(cfg);
   if (st != BEAM_OK) return st;
   if ((st = check_T(T, cfg)) != BEAM_OK) return st;
@@ -926,7 +1043,9 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
   if (T == 0) return BEAM_OK;
   if (!h_host || !x_host || !h_out_host || !y_out_host || !ws) return BEAM_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return BEAM_ERR_MISALIGNED;
-  if (ws_bytes < beam_moe_layer_host_workspace_size(cfg, T)) return BEAM_ERR_WORKSPACE_TOO_SMALL;
+  const size_t need = fp4w != nullptr ? beam_moe_layer_nvfp4_host_workspace_size(cfg, T)
+                                      : beam_moe_layer_host_workspace_size(cfg, T);
+  if (need == 0 || ws_bytes < need) return need == 0 ? BEAM_ERR_UNSUPPORTED_SHAPE : BEAM_ERR_WORKSPACE_TOO_SMALL;
   const size_t bytes = static_cast<size_t>(T) * cfg->hidden * 2;
   const size_t act = align_up(bytes);
   char* base = static_cast<char*>(ws);
@@ -958,6 +1077,10 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
       k.h_out = mho;
       k.y_out = myo;
       k.wt = *wt;
+      if (fp4w != nullptr) {
+        k.fp4w = *fp4w;
+        k.fp4 = 1;
+      }
       k.cfg = *cfg;
       k.ws = ws;
       k.ws_bytes = ws_bytes;
@@ -986,6 +1109,20 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
       return host_call_error(dev, err_slot != nullptr, s);
     }
   }
+  if (fp4w == nullptr && T >= kPipeTokens && beam::router_tc_supported((T / kPipeChunks), cfg->num_experts, cfg->hidden) &&
+      !beam::route_decode_supported(T, cfg->hidden, cfg->num_experts, cfg->num_groups, cfg->topk)) {
+    std::lock_guard<std::mutex> lock(g_aux_mu);
+    if (CopyAux* a = copy_aux(dev)) {
+      DeviceInfo d;
+      if ((st = device_info(&d)) != BEAM_OK) return st;
+      if (ws_bytes - 4 * act < layer_ws(cfg, T, d.sms).total) return BEAM_ERR_WORKSPACE_TOO_SMALL;
+      st = layer_host_pipelined(h_host, x_host, n, wt, T, cfg, h_out_host, y_out_host, d_h, d_x, d_hn, d_y,
+                                base + 4 * act, d.sms, s, a, err_slot);
+      if (st != BEAM_OK) return st;
+      if (cudaStreamSynchronize(s) != cudaSuccess) return BEAM_ERR_CUDA;
+      return host_call_error(dev, err_slot != nullptr, s);
+    }
+  }
   if (cudaMemcpyAsync(d_h, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaMemcpyAsync(d_x, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (T >= kOverlapTokens) {
@@ -995,7 +1132,7 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
       std::memset(&dbg, 0, sizeof dbg);
       dbg.stage_events[1] = a->after_boundary;  // recorded once h' is written
       st = layer_impl(d_h, d_x, n, wt, T, cfg, d_hn, d_y, &dbg, base + 4 * act, ws_bytes - 4 * act, stream, false,
-                      nullptr, err_slot);
+                      nullptr, err_slot, fp4w);
       if (st != BEAM_OK) return st;
       if (cudaStreamWaitEvent(a->side, a->after_boundary, 0) != cudaSuccess ||
           cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, a->side) != cudaSuccess ||
@@ -1008,12 +1145,31 @@ beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host
     }
   }
   st = layer_impl(d_h, d_x, n, wt, T, cfg, d_hn, d_y, nullptr, base + 4 * act, ws_bytes - 4 * act, stream, false,
-                  nullptr, err_slot);
+                  nullptr, err_slot, fp4w);
   if (st != BEAM_OK) return st;
   if (cudaMemcpyAsync(h_out_host, d_hn, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaMemcpyAsync(y_out_host, d_y, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return BEAM_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return BEAM_ERR_CUDA;
   return host_call_error(dev, err_slot != nullptr, s);
+}
+
+}  // namespace
+
+beam_status_t beam_moe_layer_host(const uint16_t* h_host, const uint16_t* x_host, int n,
+                                  const beam_moe_weights_t* wt, int T, const beam_moe_config_t* cfg,
+                                  uint16_t* h_out_host, uint16_t* y_out_host, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  return layer_host_impl(h_host, x_host, n, wt, nullptr, T, cfg, h_out_host, y_out_host, ws, ws_bytes, stream);
+}
+
+beam_status_t beam_moe_layer_nvfp4_host(const uint16_t* h_host, const uint16_t* x_host, int n,
+                                        const beam_moe_nvfp4_weights_t* weights, int T, const beam_moe_config_t* cfg,
+                                        uint16_t* h_out_host, uint16_t* y_out_host, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  if (weights == nullptr) return BEAM_ERR_INVALID_ARG;
+  const beam_moe_weights_t shared = {weights->w_post, weights->w_pre, weights->router_w, weights->bias, nullptr,
+                                     nullptr};
+  return layer_host_impl(h_host, x_host, n, &shared, weights, T, cfg, h_out_host, y_out_host, ws, ws_bytes, stream);
 }
 
 beam_status_t beam_release_host_graphs(void) {

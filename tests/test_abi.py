@@ -115,6 +115,19 @@ def test_workspace_sizes_grow_with_tokens(beam):
     T = 2048
     assert sizes[2] >= T * 8 * (2 * 5120 + 2560) * 2
     assert lib.beam_moe_layer_host_workspace_size(ctypes.byref(c), T) >= sizes[2] + 4 * T * 5120 * 2
+    fp4 = lib.beam_moe_nvfp4_workspace_size(ctypes.byref(c), T)
+    assert fp4 > 0 and lib.beam_moe_layer_nvfp4_host_workspace_size(ctypes.byref(c), T) >= fp4 + 4 * T * 5120 * 2
+
+
+def test_nvfp4_host_entry_rejects_bad_arguments(beam):
+    lib = beam.library()
+    c = _cfg(beam)
+    p16 = ctypes.c_void_p(1 << 20)
+    # no weights; then a workspace too small (checked before any device work)
+    assert lib.beam_moe_layer_nvfp4_host(p16, p16, 3, None, 4, ctypes.byref(c), p16, p16, p16, 1 << 30, None) == 1
+    w = beam.MoeNvfp4Weights()
+    assert lib.beam_moe_layer_nvfp4_host(p16, p16, 3, ctypes.byref(w), 4, ctypes.byref(c), p16, p16, p16, 64,
+                                         None) == 4
 
 
 def test_bounded_wait_check_rejects_bad_arguments(beam):

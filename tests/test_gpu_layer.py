@@ -107,11 +107,14 @@ def test_all_tokens_on_one_group():
     assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
 
 
-@pytest.mark.parametrize("T,pinned_out", [(1, True), (1, False), (8, True), (16, True), (64, True), (300, False)])
+@pytest.mark.parametrize("T,pinned_out", [(1, True), (1, False), (8, True), (16, True), (64, True), (300, False),
+                                         (2048, True), (8192, True)])
 def test_host_buffer_entry_point_matches_device_entry_point(T, pinned_out):
     # up to 8 tokens with page-locked buffers the layer reads and writes the
     # mapped host memory directly; otherwise it copies in and out (from 64
-    # tokens the copy of h' back overlaps the rest of the layer)
+    # tokens the copy of h' back overlaps the rest of the layer; from 8192 the
+    # layer is pipelined with the copies in four token chunks, whose router
+    # launches take narrower token tiles than the whole batch's)
     from beam_inputs import make_activations
     beam = beam_module()
     m = model("decode_t64")

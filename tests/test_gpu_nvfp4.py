@@ -251,3 +251,30 @@ def test_decode_routing_writes_rows_like_the_quantizer(T):
     assert beam.beam_get_device_error() == 0
     assert torch.equal(offsets, dbg["expert_offsets"])
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("T,pinned_out", [(1, True), (8, False), (64, True), (300, True)])
+def test_nvfp4_host_buffer_entry_point_matches_device(T, pinned_out):
+    """beam_moe_layer_nvfp4_host (mapped host memory up to 8 tokens with
+    page-locked buffers, copies otherwise) gives the bits of the device entry
+    point."""
+    beam = beam_module()
+    m = model("decode_t64")
+    cfg = m.cfg.with_(T=T)
+    mc = beam.make_config(cfg.H, cfg.E, cfg.G, cfg.TG, cfg.K, cfg.F, cfg.routed_scale, cfg.eps)
+    if "beam" not in _FP4_EXPERTS:
+        _FP4_EXPERTS["beam"] = beam.beam_nvfp4_quantize_experts(m.dev[0], m.dev[1], mc)
+    wt = beam.nvfp4_weights_struct(dev_bf16(m.wp_bits), dev_bf16(m.wq_bits), torch.from_numpy(m.W_r).cuda(),
+                                   torch.from_numpy(m.bias).cuda(), _FP4_EXPERTS["beam"], G_IN, G_ACT)
+    hb, xb = make_activations(cfg, batch=700 + T)
+    h_dev, y_dev, _ = beam.beam_moe_layer_nvfp4(dev_bf16(hb), dev_bf16(xb), cfg.n, wt, mc)
+    h_host = torch.from_numpy(hb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty_like(h_host)
+    y_out = torch.empty_like(h_host)
+    if pinned_out:
+        h_out, y_out = h_out.pin_memory(), y_out.pin_memory()
+    for _ in range(3):  # the second identical call captures a graph (mapped path), the third replays it
+        h_out, y = beam.beam_moe_layer_nvfp4_host(h_host, x_host, cfg.n, wt, mc, h_out_host=h_out, y_out_host=y_out)
+        assert torch.equal(y.view(torch.int16), y_dev.cpu().view(torch.int16))
+        assert torch.equal(h_out.view(torch.int16), h_dev.cpu().view(torch.int16))
