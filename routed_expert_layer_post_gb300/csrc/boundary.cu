@@ -48,6 +48,11 @@ namespace {
 using namespace norm;
 
 // ------------------------------------------------------------------ block per token
+// NCH chunks per thread: chunks c, c + blockDim.x, ... With two, the two block
+// reductions and their barriers are shared by twice the elements (the kernel
+// is issue-bound at prefill); each thread's chunks enter its double-float sum
+// in chunk order before the reduction, so the sums are exact as with one.
+template <int NCH>
 __global__ void __launch_bounds__(1024)
     boundary_block_kernel(const uint4* h, const uint4* __restrict__ x, const uint4* __restrict__ w_post,
                           const uint4* __restrict__ w_pre, int nc, F2 inv_h, float eps, ResidualCoef coef,
@@ -56,21 +61,30 @@ __global__ void __launch_bounds__(1024)
   ptx::griddep_wait();  // inputs come from the previous kernel
   ptx::griddep_launch_dependents();
   if (zero_slot != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_slot = 0;
-  const int c = threadIdx.x;  // chunk owned by this thread
   const int nwarps = blockDim.x >> 5;
-  const size_t idx = static_cast<size_t>(blockIdx.x) * nc + c;
-  const uint4 xv = x[idx];
-  const uint4 hv = h[idx];
-  const uint4 wp = w_post[c];
-  const uint4 wq = w_pre[c];
+  uint4 xv[NCH], hv[NCH];
+  size_t idx[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;  // chunk owned by this thread
+    idx[i] = static_cast<size_t>(blockIdx.x) * nc + c;
+    xv[i] = x[idx[i]];
+    hv[i] = h[idx[i]];
+  }
   F2x2 acc{{0.f, 0.f}, {0.f, 0.f}};
-  acc_squares2(acc, xv);
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) acc_squares2(acc, xv[i]);
   const F2 r = block_rsqrt_mean(fold(acc), red, nwarps, inv_h, eps);
   F2x2 acc2{{0.f, 0.f}, {0.f, 0.f}};
-  const uint4 hn = chunk_residual(xv, hv, wp, r, coef, acc2);
-  h_out[idx] = hn;
+  uint4 hn[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    hn[i] = chunk_residual(xv[i], hv[i], w_post[threadIdx.x + i * blockDim.x], r, coef, acc2);
+    h_out[idx[i]] = hn[i];
+  }
   const F2 r2 = block_rsqrt_mean(fold(acc2), red, nwarps, inv_h, eps);
-  z_out[idx] = chunk_scale(hn, wq, r2);
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) z_out[idx[i]] = chunk_scale(hn[i], w_pre[threadIdx.x + i * blockDim.x], r2);
 }
 
 // ------------------------------------------------------------------ with the combine fused in
@@ -163,8 +177,16 @@ cudaError_t launch_boundary(const uint16_t* h, const uint16_t* x, const uint16_t
   const uint4* wq = reinterpret_cast<const uint4*>(w_pre);
   uint4* ho = reinterpret_cast<uint4*>(h_out);
   uint4* zo = reinterpret_cast<uint4*>(z_out);
-  const cudaError_t err = launch_kernel(boundary_block_kernel, dim3(T), dim3(H / 8), 0, stream, pdl, hp, xp, wp, wq,
-                                        H / 8, inv_h, eps, coef, ho, zo, zero_slot);
+  // two chunks per thread from 1024 tokens when that still fills whole warps:
+  // 16384 tokens 226 -> 209 us, 2048 tokens 33 -> 31 us; at 64 tokens one
+  // chunk per thread, which keeps more loads in flight, measured 8.6 against
+  // 10.8 us
+  const bool two = T >= 1024 && H % 512 == 0;
+  const cudaError_t err =
+      two ? launch_kernel(boundary_block_kernel<2>, dim3(T), dim3(H / 16), 0, stream, pdl, hp, xp, wp, wq, H / 8, inv_h,
+                          eps, coef, ho, zo, zero_slot)
+          : launch_kernel(boundary_block_kernel<1>, dim3(T), dim3(H / 8), 0, stream, pdl, hp, xp, wp, wq, H / 8, inv_h,
+                          eps, coef, ho, zo, zero_slot);
   ++launch_counter();
   return err;
 }
