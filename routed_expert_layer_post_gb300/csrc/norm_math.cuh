@@ -94,9 +94,10 @@ __device__ __forceinline__ uint32_t scaled_bf16(float a, float b, const F2& r) {
 }
 
 // Coefficients of the residual add as fp32 pairs: sqrt(n-1) = cm_hi + cm_lo,
-// 1/sqrt(n) = c_hi + c_lo.
+// 1/sqrt(n) = c_hi + c_lo; c_bnd = c_hi 2^-20 scales the bracket of the
+// fp32 residual (residual_bracket).
 struct ResidualCoef {
-  float cm_hi, cm_lo, c_hi, c_lo;
+  float cm_hi, cm_lo, c_hi, c_lo, c_bnd;
 };
 
 // bf16 bits of (sqrt(n-1) h + y) / sqrt(n)
@@ -226,6 +227,178 @@ __device__ __forceinline__ uint4 chunk_scale(const uint4& hv, const uint4& wv, c
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// ---------------------------------------------------------------- bracketed chunks
+// The boundary kernel's form of the adaptive scheme, with fewer instructions
+// per element. Each output is bracketed by two fp32 numbers that provably
+// enclose its exact value; when both round to the same bf16 number, so does
+// the exact value (rounding is monotone), and that number is the result. The
+// pairs of an 8-element chunk OR their differences into one word, so a chunk
+// takes a single branch; a chunk left open re-checks its elements out of line
+// and sends the open ones alone to the exact paths above.
+
+// a - b per lane, one IEEE rounding each
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("{\n\t.reg .b64 pa, pb;\n\t"
+      "mov.b64 pa, {%1, %2};\n\t"
+      "mov.b64 pb, {%3, %4};\n\t"
+      "sub.rn.f32x2 %0, pa, pb;\n\t}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+  return r;
+}
+
+// acc_add2 with subtractions in place of additions of negated copies (the
+// same IEEE operations, so the same sums)
+__device__ __forceinline__ void acc_add2s(F2x2& acc, float2 v) {
+  const float2 s = __fadd2_rn(acc.hi, v);
+  const float2 bp = fsub2(s, acc.hi);
+  const float2 e = __fadd2_rn(fsub2(acc.hi, fsub2(s, bp)), fsub2(v, bp));
+  acc.hi = s;
+  acc.lo = __fadd2_rn(acc.lo, e);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
+// The products of both lanes of two bf16x2 words, exact in fp32 (8-bit
+// significands), each by one mixed-precision multiply-add straight from the
+// packed halves: no unpacking. Adding -0 keeps the sign of a zero product.
+__device__ __forceinline__ float2 mul_bf16x2(uint32_t a, uint32_t b) {
+  float2 r;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "mov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %1, ah, bh, 0f80000000;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(a), "r"(b));
+  return r;
+}
+
+// Ends of the bracket of a * b * r: the scale r.hi (1 -+ 2^-21), rounded.
+// The pair r is within 2^-45 of 1/sqrt(mean + eps) and r.hi within 2^-24 of
+// it, so the ends lie at least 2^-21.4 (relative) below and above the exact
+// scale.
+struct ScaleBracket {
+  float lo, hi;
+};
+__device__ __forceinline__ ScaleBracket scale_bracket(const F2& r) {
+  return {__fmul_rn(r.hi, 1.0f - 0x1p-21f), __fmul_rn(r.hi, 1.0f + 0x1p-21f)};
+}
+
+// Bracket of a * b * r for a pair, given the exact products ab = a * b: the
+// rounded products fl(ab s.lo) and fl(ab s.hi) keep the exact value between
+// them (each end's rounding, 2^-24, is well inside its scale's 2^-21.4
+// margin) for every result in the normal range. Returns the bf16x2 of the s.hi end;
+// open collects the bits in which the two ends' roundings differ.
+__device__ __forceinline__ uint32_t scaled_bracket(float2 ab, const ScaleBracket& s, uint32_t& open) {
+  const uint32_t lo = bf16x2_bits(__fmul2_rn(ab, make_float2(s.lo, s.lo)));
+  const uint32_t hi = bf16x2_bits(__fmul2_rn(ab, make_float2(s.hi, s.hi)));
+  open |= lo ^ hi;
+  return hi;
+}
+
+// Bracket of (sqrt(n-1) h + y) / sqrt(n) for a pair. With S = |sqrt(n-1) h| +
+// |y|, v = fl(fl(cm_hi h + y) c_hi) is within c S 2^-21.9 of the exact value
+// (two roundings and the two rounded coefficients), cancellation included;
+// v -+ fl(|h| cm_hi + |y|) c_bnd (c_bnd = c_hi 2^-20), each formed by one
+// fused multiply-add, stays beyond that after its own rounding.
+__device__ __forceinline__ uint32_t residual_bracket(float2 h, float2 y, const ResidualCoef& k, uint32_t& open) {
+  const float2 cm = make_float2(k.cm_hi, k.cm_hi);
+  const float2 v = __fmul2_rn(__ffma2_rn(cm, h, y), make_float2(k.c_hi, k.c_hi));
+  const float2 m = __ffma2_rn(abs2(h), cm, abs2(y));
+  const uint32_t lo = bf16x2_bits(__ffma2_rn(m, make_float2(-k.c_bnd, -k.c_bnd), v));
+  const uint32_t hi = bf16x2_bits(__ffma2_rn(m, make_float2(k.c_bnd, k.c_bnd), v));
+  open |= lo ^ hi;
+  return hi;
+}
+
+// an open chunk of a * b * r: each element re-checked, the open ones exact
+static __device__ __noinline__ uint4 reopen_scaled(uint4 av, uint4 bv, F2 r, ScaleBracket sb, uint4 ov) {
+  const uint32_t a[4] = {av.x, av.y, av.z, av.w};
+  const uint32_t b[4] = {bv.x, bv.y, bv.z, bv.w};
+  uint32_t o[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 pa = unpack2(a[i]), pb = unpack2(b[i]);
+    uint32_t open = 0;
+    scaled_bracket(__fmul2_rn(pa, pb), sb, open);
+    if (open & 0xffffu) o[i] = (o[i] & 0xffff0000u) | scaled_bf16(pa.x, pb.x, r);
+    if (open >> 16) o[i] = (o[i] & 0xffffu) | (scaled_bf16(pa.y, pb.y, r) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// an open chunk of the residual add: each element re-checked, the open ones exact
+static __device__ __noinline__ uint4 reopen_residual(uint4 hv, uint4 yv, ResidualCoef k, uint4 ov) {
+  const uint32_t h[4] = {hv.x, hv.y, hv.z, hv.w};
+  const uint32_t y[4] = {yv.x, yv.y, yv.z, yv.w};
+  uint32_t o[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 ph = unpack2(h[i]), py = unpack2(y[i]);
+    uint32_t open = 0;
+    residual_bracket(ph, py, k, open);
+    if (open & 0xffffu) o[i] = (o[i] & 0xffff0000u) | residual_bf16(ph.x, py.x, k);
+    if (open >> 16) o[i] = (o[i] & 0xffffu) | (residual_bf16(ph.y, py.y, k) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// bf16 of a * b * r for a chunk (sb = scale_bracket(r))
+__device__ __forceinline__ uint4 chunk_scaled(const uint4& av, const uint4& bv, const F2& r, const ScaleBracket& sb) {
+  uint32_t open = 0;
+  const uint4 o = make_uint4(scaled_bracket(mul_bf16x2(av.x, bv.x), sb, open),
+                             scaled_bracket(mul_bf16x2(av.y, bv.y), sb, open),
+                             scaled_bracket(mul_bf16x2(av.z, bv.z), sb, open),
+                             scaled_bracket(mul_bf16x2(av.w, bv.w), sb, open));
+  return open == 0 ? o : reopen_scaled(av, bv, r, sb, o);
+}
+
+// y = bf16(x w_post r), then h' = bf16((sqrt(n-1) h + y) / sqrt(n)) for a
+// chunk; returns h' and accumulates its squares (in element order, as
+// chunk_residual)
+__device__ __forceinline__ uint4 chunk_residual_bracketed(const uint4& xv, const uint4& hv, const uint4& wv,
+                                                          const F2& r, const ScaleBracket& sb, const ResidualCoef& k,
+                                                          F2x2& acc) {
+  const uint4 y = chunk_scaled(xv, wv, r, sb);
+  uint32_t open = 0;
+  uint4 o = make_uint4(residual_bracket(unpack2(hv.x), unpack2(y.x), k, open),
+                       residual_bracket(unpack2(hv.y), unpack2(y.y), k, open),
+                       residual_bracket(unpack2(hv.z), unpack2(y.z), k, open),
+                       residual_bracket(unpack2(hv.w), unpack2(y.w), k, open));
+  if (open != 0) o = reopen_residual(hv, y, k, o);
+  const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc_add2s(acc, mul_bf16x2(w[i], w[i]));
+  return o;
+}
+
+// squares of a chunk of bf16 values into a pair of double-float sums
+__device__ __forceinline__ void acc_squares2s(F2x2& acc, const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc_add2s(acc, mul_bf16x2(w[i], w[i]));
+}
+
+// block_rsqrt_mean without the closing barrier: each of the kernel's
+// reductions has a red array of its own
+__device__ __forceinline__ F2 block_rsqrt_mean_once(F2 v, F2* red, int nwarps, F2 inv_h, float eps) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  v = warp_sum_f2(v);
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    F2 t = (lane < nwarps) ? red[lane] : F2{0.f, 0.f};
+    t = warp_sum_f2(t);
+    if (lane == 0) red[32] = rsqrt_mean(t, inv_h, eps);
+  }
+  __syncthreads();
+  return red[32];
+}
+
 // block-wide sum of squares -> 1/sqrt(mean + eps), evaluated by one thread;
 // red needs 33 entries
 __device__ __forceinline__ F2 block_rsqrt_mean(F2 v, F2* red, int nwarps, F2 inv_h, float eps) {
@@ -259,6 +432,7 @@ inline ResidualCoef residual_coef(int n) {
   coef.cm_lo = static_cast<float>(cm - static_cast<double>(coef.cm_hi));
   coef.c_hi = static_cast<float>(c);
   coef.c_lo = static_cast<float>(c - static_cast<double>(coef.c_hi));
+  coef.c_bnd = std::ldexp(coef.c_hi, -20);
   return coef;
 }
 
