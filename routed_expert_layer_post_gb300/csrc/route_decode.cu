@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                         int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_perm, uint4* __restrict__ x_perm,
                         uint8_t* __restrict__ xq, uint4* __restrict__ xsf, float g_in, int* sync,
                         int* __restrict__ clear, int clear_ints) {
-  __shared__ F2 red[33];
+  __shared__ F2 red[2][33];  // one per norm reduction
   __shared__ float fred[32], fred2[32];
   __shared__ int hist[256];
   __shared__ int s_pos[kMaxPairs];
@@ -190,12 +190,24 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const uint4 xv = x[idx];
       const uint4 hv = h[idx];
       F2x2 acc{{0.f, 0.f}, {0.f, 0.f}};
-      acc_squares2(acc, xv);
-      const F2 r = block_rsqrt_mean(fold(acc), red, nwarps, inv_h, eps);
       F2x2 acc2{{0.f, 0.f}, {0.f, 0.f}};
-      hc[t] = chunk_residual(xv, hv, wp, r, coef, acc2);
-      const F2 r2 = block_rsqrt_mean(fold(acc2), red, nwarps, inv_h, eps);
-      zc[t] = chunk_scale(hc[t], wq, r2);
+      if constexpr (TMAX <= 4) {
+        // the boundary kernel's bracketed chunks (the same bits); red[0] is
+        // written again only after the next reduction's barriers
+        acc_squares2s(acc, xv);
+        const F2 r = block_rsqrt_mean_once(fold(acc), red[0], nwarps, inv_h, eps);
+        hc[t] = chunk_residual_bracketed(xv, hv, wp, r, scale_bracket(r), coef, acc2);
+        const F2 r2 = block_rsqrt_mean_once(fold(acc2), red[1], nwarps, inv_h, eps);
+        zc[t] = chunk_scaled(hc[t], wq, r2, scale_bracket(r2));
+      } else {
+        // per-pair checks: with eight tokens' h' and z held in registers the
+        // out-of-line calls of the bracketed form spill
+        acc_squares2(acc, xv);
+        const F2 r = block_rsqrt_mean(fold(acc), red[0], nwarps, inv_h, eps);
+        hc[t] = chunk_residual(xv, hv, wp, r, coef, acc2);
+        const F2 r2 = block_rsqrt_mean(fold(acc2), red[0], nwarps, inv_h, eps);
+        zc[t] = chunk_scale(hc[t], wq, r2);
+      }
       // router logits of the block's experts: z . W_r[e] in fp32 FMA, fixed reduction order
       float zf[8];
       unpack8(zc[t], zf);
