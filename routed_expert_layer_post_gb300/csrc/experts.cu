@@ -83,7 +83,6 @@ struct PhaseParams {
   CUtensorMap tmap_w;   // weights, 3-D: (k, row, plane); expert e owns planes e*planes .. +planes-1
   CUtensorMap tmap_x;   // activations, 2-D: (k, permuted row)
   CUtensorMap tmap_sfx; // NVFP4: activation scale slots, 2-D: (16-byte slot, permuted row)
-  CUtensorMap tmap_x16; // paired-SM GEMMs: activations with a 16-row box (narrow last token tiles)
   uint16_t* out;        // bf16 output (down; gate/up of the bf16 path)
   uint8_t* out_q;       // NVFP4 gate/up: codes of the SwiGLU output [rows][F/2]
   uint8_t* out_sf;      // NVFP4 gate/up: its scale slots [rows][F/64][16]
@@ -1130,14 +1129,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
 // the epilogue pairs them through shared memory for SwiGLU. A pair covers 128 d_ff columns. Down: 128
 // rows of W_d per CTA, 256 per pair.
 //
-// Narrow last tiles: an expert's rows rarely fill its last 256-token tile
-// (at 16384 tokens and 256 experts, 256-wide tiles would compute 19 % empty
-// columns). That tile runs as an MMA of width N = its rows rounded up to 32;
-// each CTA then supplies N/2 token rows (CTA 0 the first half, CTA 1 the
-// second, so accumulator column c is still the tile's token c), loaded as
-// 16-row boxes.
+// Tile widths: an expert's rows rarely fill whole 256-token tiles (at 16384
+// tokens and 256 experts, 256-wide tiles would compute 19 % empty columns).
+// Its rows are cut into ceil(rows / 256) tiles of one width, a multiple of 32
+// (pair_tile_width), and each runs as an MMA of width N = its rows rounded up
+// to 32; each CTA then supplies N/2 token rows (CTA 0 the first half, CTA 1
+// the second, so accumulator column c is still the tile's token c), from one
+// 128-row box.
 //
-// Work: tiles (expert, weight row block, 256-token tile) from the launch's
+// Work: tiles (expert, weight row block, token tile) from the launch's
 // unit counter, taken by the leader and published to both CTAs' queues (no
 // tile waits on another). Roles (320 threads): warp 0 loads this CTA's
 // halves; warp 1 of the leader CTA (cluster rank 0) issues the MMAs of a stage
@@ -1152,11 +1152,22 @@ constexpr int kPairStages = (kSmemLimit - 1024 - kCtrlBytes - kPairXchBytes) / k
 constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + kPairXchBytes + kCtrlBytes;
 constexpr int kPairTmemCols = 2 * kPairN;                          // two accumulator buffers
 
-// MMA width (tokens) of a tile holding `valid` rows: the full 256, or for an
-// expert's last, partly filled tile the rows rounded up to 32, so that the
-// tensor cores skip the empty columns (each CTA then loads and supplies half
-// of the width, 16 rows per TMA box).
+// MMA width (tokens) of a tile holding `valid` rows: the rows rounded up to
+// 32, at most 256, so that the tensor cores skip empty columns; each CTA
+// supplies half of the width.
 __device__ __forceinline__ int pair_width(int valid) { return valid >= kPairN ? kPairN : (valid + 31) & ~31; }
+
+// Token tiles of an expert with R rows: ceil(R / 256) tiles of one width, R
+// over the tile count rounded up to 32 (the last tile takes the rest), e.g.
+// 600 rows as 224 + 224 + 152 rather than 256 + 256 + 88. Every tile streams
+// a whole weight tile, so balanced widths spread the MMA work evenly over
+// them. The width is at most 256 and every tile holds at least one row (a
+// width below 256 means at most seven tiles, and seven 32-row roundings fit
+// in the rows past the first tile).
+__device__ __forceinline__ int pair_tile_width(const int* s_off, const int* s_ntt, int e) {
+  const int nt = s_ntt[e];
+  return ((s_off[e + 1] - s_off[e] + nt - 1) / nt + 31) & ~31;
+}
 static_assert(kPairStages >= 6, "six 32 KB stages per SM");
 
 // Bounded wait at cluster scope (for barriers the other CTA arrives on).
@@ -1226,7 +1237,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&ph.tmap_w);
     ptx::prefetch_tensormap(&ph.tmap_x);
-    ptx::prefetch_tensormap(&ph.tmap_x16);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(tmem_slot, kPairTmemCols);
@@ -1318,10 +1328,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (u < 0 || !ok) break;
         }
         const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
-        const int base_row = s_off[w.e] + w.tt * kPairN;
-        const int half = pair_width(s_off[w.e + 1] - base_row) / 2;  // token rows this CTA supplies
+        const int tw = pair_tile_width(s_off, s_ntt, w.e);
+        const int base_row = s_off[w.e] + w.tt * tw;
+        const int half = pair_width(min(tw, s_off[w.e + 1] - base_row)) / 2;  // token rows this CTA supplies
         const int row0 = base_row + static_cast<int>(rank) * half;
-        const uint32_t stage_tx = 2u * static_cast<uint32_t>(kTileABytes + half * kBK * 2);
+        // one 128-row box per CTA whatever the width: the MMA reads the first
+        // `half` rows. A box per 16 rows cost the producer one TMA
+        // instruction per 16 rows (16384 tokens: both GEMMs 3-4 % slower).
+        constexpr uint32_t stage_tx = 2u * static_cast<uint32_t>(kPairStageBytes);
         for (int k = 0; k < ph.ksteps; ++k) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, 31, kTimeoutNs)) {
             ok = false;
@@ -1339,12 +1353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::tma_load_3d_pair(st, &ph.tmap_w, fb, k * kBK, w.mb * 2 * kBM + static_cast<int>(rank) * kBM, w.e,
                                   pol_w);
           }
-          if (half == kPairRows) {
-            ptx::tma_load_2d_pair(st + kTileABytes, &ph.tmap_x, fb, k * kBK, row0, pol_x);
-          } else {
-            for (int i = 0; i < half; i += 16)
-              ptx::tma_load_2d_pair(st + kTileABytes + i * kBK * 2, &ph.tmap_x16, fb, k * kBK, row0 + i, pol_x);
-          }
+          ptx::tma_load_2d_pair(st + kTileABytes, &ph.tmap_x, fb, k * kBK, row0, pol_x);
           ++issued;
           if (++stage == kPairStages) {
             stage = 0;
@@ -1372,8 +1381,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(&qempty[slot]);
         if (u < 0) break;
         const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
-        const int base_row = s_off[w.e] + w.tt * kPairN;
-        const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, pair_width(s_off[w.e + 1] - base_row));
+        const int tw = pair_tile_width(s_off, s_ntt, w.e);
+        const int base_row = s_off[w.e] + w.tt * tw;
+        const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, pair_width(min(tw, s_off[w.e + 1] - base_row)));
         if (!wait_bar_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, 33)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
@@ -1434,8 +1444,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (u < 0) break;
       ptx::tc_fence_after();
       const Unit w = decode_unit(u, n_units, p, s_ttstart, s_ntt);
-      const int row0 = s_off[w.e] + w.tt * kPairN;
-      const int valid = min(kPairN, s_off[w.e + 1] - row0);
+      const int tw = pair_tile_width(s_off, s_ntt, w.e);
+      const int row0 = s_off[w.e] + w.tt * tw;
+      const int valid = min(tw, s_off[w.e + 1] - row0);
       const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(eg * kPairN);
       for (int c0 = 0; c0 < valid; c0 += 16) {
         uint32_t r[16];
@@ -2014,8 +2025,6 @@ cudaError_t launch_gemm_pair(int mode, const uint16_t* weights, const uint16_t* 
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kdim) * 2};
     const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(kPairRows)};
     if (!encode_map(&ph.tmap_x, act_in, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    const cuuint32_t box16[2] = {kBK, 16};
-    if (!encode_map(&ph.tmap_x16, act_in, 2, dims, strides, box16)) return cudaErrorInvalidValue;
   }
   ph.out = out;
   ph.n_mb = mode == 0 ? F / kBM : H / (2 * kBM);
