@@ -23,7 +23,7 @@ def limit_model() -> Model:
     return Model(BeamConfig("limits", T=40, H=8192, E=64, G=8, TG=4, K=16, F=256, n=7))
 
 
-@pytest.mark.parametrize("T", [1, 37])
+@pytest.mark.parametrize("T", [1, 37, 1030])  # 1030: two chunks per thread from 1024 tokens
 def test_boundary_at_the_largest_hidden_size(T):
     beam = beam_module()
     cfg = limit_model().cfg.with_(T=T)
