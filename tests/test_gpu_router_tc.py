@@ -14,7 +14,8 @@ from tests.gpu_support import beam_module, dev_bf16, f64_of, model
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T", [129, 1000, 2048])
+# token tiles of 32 (up to 4863 tokens), 64 (5000) and 128 (10000)
+@pytest.mark.parametrize("T", [129, 1000, 2048, 5000, 10000])
 def test_layer_tc_router_matches_fp64(T):
     beam = beam_module()
     m = model("decode_t64")
