@@ -898,15 +898,19 @@ bool capture_graph(HostGraph* g) {
 // kOverlapTokens tokens up, h' (final once the boundary has run) is copied
 // back on the side stream while the rest of the layer computes. From
 // kPipeTokens tokens up the layer is pipelined with the copies in
-// kPipeChunks token chunks (layer_host_pipelined).
+// pipe_chunks(T) token chunks (layer_host_pipelined).
 constexpr int kOverlapTokens = 64;
 constexpr int kPipeTokens = 8192;  // measured: 16384 tokens e2e 10.70 -> 10.39 ms; 2048 tokens 3.58 -> 3.69 ms (not used there)
-constexpr int kPipeChunks = 4;
+constexpr int kPipeMaxChunks = 8;
+// chunks of at least 2048 tokens: four from 8192 tokens, eight from 16384,
+// so that less of the routing waits for the last chunk's copy and less of
+// the output's copy waits for the last combine
+constexpr int pipe_chunks(int T) { return T >= 16384 ? 8 : 4; }
 
 struct CopyAux {
   cudaStream_t side = nullptr, side_in = nullptr;
   cudaEvent_t after_boundary = nullptr, h_copied = nullptr;
-  cudaEvent_t in_done[kPipeChunks] = {}, bnd_done[kPipeChunks] = {}, y_done[kPipeChunks] = {};
+  cudaEvent_t in_done[kPipeMaxChunks] = {}, bnd_done[kPipeMaxChunks] = {}, y_done[kPipeMaxChunks] = {};
   bool ok = false;
 };
 
@@ -920,7 +924,7 @@ CopyAux* copy_aux(int dev) {
               cudaStreamCreateWithFlags(&a.side_in, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&a.after_boundary, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&a.h_copied, cudaEventDisableTiming) == cudaSuccess;
-    for (int c = 0; ok && c < kPipeChunks; ++c)
+    for (int c = 0; ok && c < kPipeMaxChunks; ++c)
       ok = cudaEventCreateWithFlags(&a.in_done[c], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&a.bnd_done[c], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&a.y_done[c], cudaEventDisableTiming) == cudaSuccess;
@@ -934,7 +938,7 @@ CopyAux* copy_aux(int dev) {
 }
 
 // Large batches through host buffers, pipelined with the copies: the
-// tokens arrive in kPipeChunks chunks on a copy-in stream, and each chunk's
+// tokens arrive in pipe_chunks(T) chunks on a copy-in stream, and each chunk's
 // boundary, router and top-k run (on the call's stream) while the next chunk
 // is still being copied; h' goes back on the side stream once the last
 // chunk's boundary has run. The permutation and the expert GEMMs take the
@@ -965,27 +969,28 @@ beam_status_t layer_host_pipelined(const uint16_t* h_host, const uint16_t* x_hos
   const ExpertsWs xw = experts_ws(cfg, T, sms);
   const uint16_t* y_perm = reinterpret_cast<const uint16_t*>(ews + xw.y_perm);
   const size_t row = static_cast<size_t>(H) * 2;
-  auto t0 = [&](int c) { return static_cast<int>(static_cast<long long>(T) * c / kPipeChunks); };
+  const int nch = pipe_chunks(T);
+  auto t0 = [&](int c) { return static_cast<int>(static_cast<long long>(T) * c / nch); };
   cudaError_t e = cudaSuccess;
   launch_counter() = 0;
   // the copy-in stream starts after everything queued on the call's stream before this call
   if ((e = cudaEventRecord(a->h_copied, s)) != cudaSuccess || (e = cudaStreamWaitEvent(a->side_in, a->h_copied, 0)) != cudaSuccess)
     return BEAM_ERR_CUDA;
-  for (int c = 0; c < kPipeChunks; ++c) {
+  for (int c = 0; c < nch; ++c) {
     const size_t o = static_cast<size_t>(t0(c)) * H, bytes = static_cast<size_t>(t0(c + 1) - t0(c)) * row;
     if (cudaMemcpyAsync(d_h + o, h_host + o, bytes, cudaMemcpyHostToDevice, a->side_in) != cudaSuccess ||
         cudaMemcpyAsync(d_x + o, x_host + o, bytes, cudaMemcpyHostToDevice, a->side_in) != cudaSuccess ||
         cudaEventRecord(a->in_done[c], a->side_in) != cudaSuccess)
       return BEAM_ERR_CUDA;
   }
-  for (int c = 0; c < kPipeChunks; ++c) {
+  for (int c = 0; c < nch; ++c) {
     const int tc = t0(c + 1) - t0(c);
     const size_t o = static_cast<size_t>(t0(c)) * H;
     if (cudaStreamWaitEvent(s, a->in_done[c], 0) != cudaSuccess) return BEAM_ERR_CUDA;
     e = beam::launch_boundary(d_h + o, d_x + o, wt->w_post, wt->w_pre, tc, H, cfg->eps, n, d_hn + o, z + o, s,
                               /*pdl=*/false, c == 0 ? router_ticket : nullptr);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
-    if (c == kPipeChunks - 1) {
+    if (c == nch - 1) {
       // h' goes back once the copies in are done: the link then carries it
       // alongside the expert GEMMs instead of slowing the incoming chunks
       if (cudaEventRecord(a->bnd_done[c], s) != cudaSuccess ||
@@ -1011,7 +1016,7 @@ beam_status_t layer_host_pipelined(const uint16_t* h_host, const uint16_t* x_hos
   beam_status_t st = run_experts(x_perm, offsets, wt->w_gate_up, wt->w_down, w, inv, T, cfg, nullptr, ews, sms, s,
                                  nullptr, true, /*cleared=*/true, nullptr, nullptr);
   if (st != BEAM_OK) return st;
-  for (int c = 0; c < kPipeChunks; ++c) {
+  for (int c = 0; c < nch; ++c) {
     const int tc = t0(c + 1) - t0(c);
     const size_t o = static_cast<size_t>(t0(c)) * H, ko = static_cast<size_t>(t0(c)) * K;
     e = beam::launch_combine(y_perm, w + ko, inv + ko, tc, K, H, d_y + o, s, /*pdl=*/true,
@@ -1109,7 +1114,7 @@ beam_status_t layer_host_impl(const uint16_t* h_host, const uint16_t* x_host, in
       return host_call_error(dev, err_slot != nullptr, s);
     }
   }
-  if (fp4w == nullptr && T >= kPipeTokens && beam::router_tc_supported((T / kPipeChunks), cfg->num_experts, cfg->hidden) &&
+  if (fp4w == nullptr && T >= kPipeTokens && beam::router_tc_supported(T / pipe_chunks(T), cfg->num_experts, cfg->hidden) &&
       !beam::route_decode_supported(T, cfg->hidden, cfg->num_experts, cfg->num_groups, cfg->topk)) {
     std::lock_guard<std::mutex> lock(g_aux_mu);
     if (CopyAux* a = copy_aux(dev)) {

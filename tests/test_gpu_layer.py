@@ -108,13 +108,14 @@ def test_all_tokens_on_one_group():
 
 
 @pytest.mark.parametrize("T,pinned_out", [(1, True), (1, False), (8, True), (16, True), (64, True), (300, False),
-                                         (2048, True), (8192, True)])
+                                         (2048, True), (8192, True), (16384, True)])
 def test_host_buffer_entry_point_matches_device_entry_point(T, pinned_out):
     # up to 8 tokens with page-locked buffers the layer reads and writes the
     # mapped host memory directly; otherwise it copies in and out (from 64
     # tokens the copy of h' back overlaps the rest of the layer; from 8192 the
-    # layer is pipelined with the copies in four token chunks, whose router
-    # launches take narrower token tiles than the whole batch's)
+    # layer is pipelined with the copies in four token chunks, eight from
+    # 16384, whose router launches take narrower token tiles than the whole
+    # batch's)
     from beam_inputs import make_activations
     beam = beam_module()
     m = model("decode_t64")
