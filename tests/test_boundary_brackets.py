@@ -140,3 +140,57 @@ def test_residual_bracket_near_cancellation(n):
         zero = ref == 0
         assert zero.any()
         assert not (lo == hi)[zero & (h != 0)].any()
+
+
+# ---------------------------------------------------------------- per-pair checks
+# The decode routing kernel with eight tokens keeps the earlier per-element
+# checks: v = fl(ab r_hi) with the interval fl(v -+ fl(|v| 2^-21)) for y and
+# z, and v = fl(fl(cm_hi h + y) c_hi) with fl(v -+ e), e = fl(fl(fl(|fl(cm_hi
+# h)| + |y|) c_hi) 2^-20), for h'.
+
+def scaled_interval(a, b, r):
+    ab = (a * b).astype(F32)
+    v = (ab * r.astype(F32)).astype(F32)
+    e = (np.abs(v) * F32(2.0 ** -21)).astype(F32)
+    return bf16_bits_of_f32(v - e), bf16_bits_of_f32(v + e), bf16_bits_of_f32(v)
+
+
+def residual_interval(h, y, n):
+    cm, c = np.sqrt(n - 1.0), 1.0 / np.sqrt(float(n))
+    cm_hi, c_hi = F32(cm), F32(c)
+    ch = (cm_hi * h.astype(F32)).astype(F32)
+    v = (fma32(cm_hi, h, y) * c_hi).astype(F32)
+    e = (((np.abs(ch) + np.abs(y).astype(F32)).astype(F32) * c_hi).astype(F32) * F32(2.0 ** -20)).astype(F32)
+    ref = (cm * h + y) * c
+    err = 8 * 2.0 ** -53 * (np.abs(cm * h) + np.abs(y)) * c
+    return bf16_bits_of_f32(v - e), bf16_bits_of_f32(v + e), bf16_bits_of_f32(v), ref, err
+
+
+def test_per_pair_scaled_check():
+    rng = np.random.default_rng(7)
+    n = 1_000_000
+    a = random_bf16(rng, n, -8, 8)
+    b = obf.round_bf16(1.0 + 0.02 * rng.standard_normal(n))
+    t = random_bf16(rng, n, -8, 8)
+    t = np.where(t == 0, 1.0, t)
+    _, ex = np.frexp(t)
+    mid = t + np.copysign(np.ldexp(1.0, ex - 9), t)
+    near = np.abs(mid / (a * b)) * (1.0 + rng.uniform(-2.0 ** -18, 2.0 ** -18, n))
+    r = np.where(rng.random(n) < 0.5, near, np.exp2(rng.uniform(-12, 12, n)))
+    ok = np.isfinite(r) & (r > 0)
+    a, b, r = a[ok], b[ok], r[ok]
+    lo, hi, val = scaled_interval(a, b, r)
+    closed = lo == hi
+    assert np.array_equal(val[closed], obf.encode(a * b * r)[closed])
+
+
+@pytest.mark.parametrize("n", [5, 20, 100])
+def test_per_pair_residual_check(n):
+    rng = np.random.default_rng(200 + n)
+    m = 500_000
+    h = random_bf16(rng, m, -6, 6)
+    d = rng.uniform(-2.0 ** -6, 2.0 ** -6, m)
+    y = np.where(rng.random(m) < 0.5, obf.round_bf16(-np.sqrt(n - 1.0) * h * (1.0 + d)), random_bf16(rng, m, -6, 6))
+    lo, hi, val, ref, err = residual_interval(h, y, n)
+    use = (lo == hi) & decided(ref, err)
+    assert np.array_equal(val[use], obf.encode(ref[use]))
